@@ -1,0 +1,173 @@
+"""Oracle: plain fp64 CPU restatement of the FLUX.2 joint RoPE attention.
+
+TEST INFRASTRUCTURE ONLY. The test-suite, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` are the only
+callers. The product path never imports this package, and this package
+imports nothing from the product package.
+
+The arithmetic lives in ``flux_oracle.c`` (compiled with gcc, no fast-math);
+this file only builds it and marshals numpy arrays. The one step done here is
+the concatenation of the text and image position ids into the joint sequence
+[txt ; img] ("Diffusers 中 Flux2Transformer2DModel 全面解析", section
+"前向传播输入输出约定": both id sets are 4-d (T, H, W, L) and the text and
+image streams are attended jointly; "FLUX.2 [klein]" survey page, section
+"模型架构": reference-image tokens are concatenated with the noisy tokens).
+
+Pins (tests/test_oracle_pins.py): zero ids give the identity, rotations keep
+norms, the post-RoPE dot product depends only on the id difference, the
+per-axis frequencies match theta^(-2j/d_a) evaluated independently at high
+precision, a complex-number brute force agrees, identical keys give the mean
+of V, and the attention agrees with torch's float64 SDPA and with a naive
+Python triple loop on tiny inputs. No function is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "flux_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_default = None
+
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-fno-fast-math",
+             "-ffp-contract=off"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc-compile an oracle C source into a shared library at ``out``."""
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *GCC_FLAGS, src, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile flux_oracle.c into oracle/_build/liboracle.so (gcc -O2, IEEE fp64)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE))
+    if force or stale:
+        compile_source(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def joint_ids(txt_ids, img_ids) -> np.ndarray:
+    """Position ids of the joint sequence: text tokens first, then image tokens."""
+    parts = [np.asarray(x, dtype=np.int32).reshape(-1, np.asarray(x).shape[-1])
+             for x in (txt_ids, img_ids) if x is not None and np.asarray(x).size > 0]
+    return np.ascontiguousarray(np.concatenate(parts, axis=0), dtype=np.int32)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+class Oracle:
+    """The oracle's entry points bound to one compiled library."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        P = ctypes.c_void_p
+        lib.oracle_rope_tables.argtypes = [P, ctypes.c_int64, P, ctypes.c_int,
+                                           ctypes.c_double, P, P]
+        lib.oracle_rope_tables.restype = ctypes.c_int
+        lib.oracle_rope_apply.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                          ctypes.c_int, P, P, P]
+        lib.oracle_rope_apply.restype = None
+        lib.oracle_joint_rope_attention.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+            P, P, ctypes.c_int, ctypes.c_double, P, ctypes.c_int64, ctypes.c_int, P]
+        lib.oracle_joint_rope_attention.restype = ctypes.c_int
+        self.lib = lib
+        self.path = lib_path
+
+    def rope_tables(self, ids, axes_dims=(32, 32, 32, 32), theta=2000.0):
+        """cos, sin tables [S, sum(axes_dims)/2] in fp64 for ids [S, n_axes]."""
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        axes = np.ascontiguousarray(axes_dims, dtype=np.int32)
+        S, n_axes = ids.shape
+        assert n_axes == axes.size
+        P = int(axes.sum()) // 2
+        c = np.empty((S, P), dtype=np.float64)
+        s = np.empty((S, P), dtype=np.float64)
+        rc = self.lib.oracle_rope_tables(_ptr(ids), S, _ptr(axes), n_axes, float(theta),
+                                         _ptr(c), _ptr(s))
+        if rc != 0:
+            raise ValueError("oracle_rope_tables: every axis width must be positive and even")
+        return c, s
+
+    def rope_apply(self, x, cos_t, sin_t):
+        """Rotate x [B, S, H, D] (fp64) with tables [S, D/2]."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        B, S, H, D = x.shape
+        cos_t = np.ascontiguousarray(cos_t, dtype=np.float64)
+        sin_t = np.ascontiguousarray(sin_t, dtype=np.float64)
+        assert cos_t.shape == (S, D // 2) and sin_t.shape == (S, D // 2)
+        y = np.empty_like(x)
+        self.lib.oracle_rope_apply(_ptr(x), B, S, H, D, _ptr(cos_t), _ptr(sin_t), _ptr(y))
+        return y
+
+    def joint_rope_attention(self, q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),
+                             theta=2000.0, rows=None, threads=None):
+        """out[b, r, h, :] for the query tokens ``rows`` (all when None).
+
+        q, k, v: [B, S, H, D] arrays (any float dtype; converted exactly to fp64).
+        Returns fp64 [B, len(rows), H, D].
+        """
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        B, S, H, D = q.shape
+        assert k.shape == q.shape and v.shape == q.shape
+        ids = joint_ids(txt_ids, img_ids)
+        assert ids.shape[0] == S, (ids.shape, S)
+        axes = np.ascontiguousarray(axes_dims, dtype=np.int32)
+        if rows is None:
+            rows_arr = np.arange(S, dtype=np.int64)
+        else:
+            rows_arr = np.ascontiguousarray(rows, dtype=np.int64)
+            assert rows_arr.size == 0 or (rows_arr.min() >= 0 and rows_arr.max() < S)
+        out = np.zeros((B, rows_arr.size, H, D), dtype=np.float64)
+        if rows_arr.size == 0:
+            return out
+        n_threads = int(threads) if threads else default_threads()
+        rc = self.lib.oracle_joint_rope_attention(
+            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+            float(theta), _ptr(rows_arr), rows_arr.size, n_threads, _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_joint_rope_attention: sum(axes_dims) must equal D, "
+                             "sizes > 0")
+        return out
+
+
+def default() -> Oracle:
+    global _default
+    with _lock:
+        if _default is None:
+            _default = Oracle(build())
+    return _default
+
+
+def rope_tables(ids, axes_dims=(32, 32, 32, 32), theta=2000.0):
+    return default().rope_tables(ids, axes_dims, theta)
+
+
+def rope_apply(x, cos_t, sin_t):
+    return default().rope_apply(x, cos_t, sin_t)
+
+
+def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),
+                         theta=2000.0, rows=None, threads=None):
+    return default().joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims, theta,
+                                          rows, threads)

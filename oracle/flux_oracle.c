@@ -1,0 +1,205 @@
+/*
+ * Oracle for the FLUX.2 joint RoPE attention: plain, slow, fp64, CPU only.
+ *
+ * TEST INFRASTRUCTURE. Only the test-suite, the smoke check and the timed
+ * CPU baseline of the bench load this file's library. The product path (the
+ * CUDA library under diffusion_transformer_joint_gb300/csrc) shares no code,
+ * header, table or constant with it.
+ *
+ * What it computes, written out from the definitions on the pages:
+ *
+ *   1. Position ids. Every token carries one id per RoPE axis; FLUX.2 uses
+ *      four axes (T, H, W, L), and the id tensor's last dimension must equal
+ *      the number of axes. Text ids come first, then image (and reference)
+ *      ids: the joint sequence is [txt ; img].
+ *      ("Diffusers 中 Flux2Transformer2DModel 全面解析", section
+ *      "前向传播输入输出约定": 4-d (T,H,W,L) ids, last dim = len(axes_dims_rope).)
+ *
+ *   2. N-D RoPE (EmbedND / Flux2PosEmbed): a 1-D RoPE is built per axis and
+ *      the axes are concatenated; axes_dims = (32,32,32,32), theta = 2000.
+ *      (Same page, sections "前向传播输入输出约定" and "模型配置参数全解";
+ *      "FLUX.2 [klein]" survey page, section "模型架构".)
+ *      Per axis a with width d_a and pair j < d_a/2 the frequency is
+ *      omega_j = theta^(-2j/d_a) and the angle is id[a] * omega_j; pair j of
+ *      axis a is the channel pair (2p, 2p+1) with p = (sum_{a'<a} d_a'/2) + j.
+ *      The pair (x_2p, x_2p+1) is multiplied, as a complex number
+ *      x_2p + i x_2p+1, by exp(i * angle).
+ *
+ *   3. Attention ("Transformer架构解析FLUX.2-klein-base-9b-nvfp4", section 2
+ *      "核心引擎自注意力机制如何工作": scaled dot-product attention):
+ *      out_i = sum_j softmax_j(q^_i . k^_j / sqrt(d)) v_j over all S tokens,
+ *      non-causal, per batch element and head, d = head_dim = 128, with q^ and
+ *      k^ the RoPE-rotated queries and keys; V is not rotated.
+ *
+ * Layout: q, k, v, out are [B, S, H, D] row-major (D fastest), in double.
+ * ids are [S, n_axes] int32 and are shared by every batch element.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Frequencies and per-token angles, step 2 above. cos_out/sin_out are
+ * [S, P] with P = sum(axes_dims)/2. Returns 0, or -1 on a bad axis width. */
+int oracle_rope_tables(const int32_t *ids, int64_t S, const int32_t *axes_dims,
+                       int n_axes, double theta, double *cos_out,
+                       double *sin_out) {
+  int P = 0;
+  for (int a = 0; a < n_axes; ++a) {
+    if (axes_dims[a] <= 0 || axes_dims[a] % 2 != 0) return -1;
+    P += axes_dims[a] / 2;
+  }
+  for (int64_t s = 0; s < S; ++s) {
+    int p = 0;
+    for (int a = 0; a < n_axes; ++a) {
+      int d_a = axes_dims[a];
+      for (int j = 0; j < d_a / 2; ++j, ++p) {
+        double omega = pow(theta, -2.0 * (double)j / (double)d_a);
+        double angle = (double)ids[s * n_axes + a] * omega;
+        cos_out[s * P + p] = cos(angle);
+        sin_out[s * P + p] = sin(angle);
+      }
+    }
+  }
+  return 0;
+}
+
+/* Rotation of one head vector x[D] by the token's table row, step 2 above:
+ * (x_2p + i x_2p+1) * (c_p + i s_p). */
+void oracle_rope_apply_vec(const double *x, const double *c, const double *sn,
+                           int D, double *y) {
+  for (int p = 0; p < D / 2; ++p) {
+    double re = x[2 * p], im = x[2 * p + 1];
+    y[2 * p] = re * c[p] - im * sn[p];
+    y[2 * p + 1] = re * sn[p] + im * c[p];
+  }
+}
+
+/* Rotation of a whole [B, S, H, D] tensor with tables [S, D/2]. */
+void oracle_rope_apply(const double *x, int B, int64_t S, int H, int D,
+                       const double *cos_t, const double *sin_t, double *y) {
+  for (int b = 0; b < B; ++b)
+    for (int64_t s = 0; s < S; ++s)
+      for (int h = 0; h < H; ++h) {
+        int64_t off = (((int64_t)b * S + s) * H + h) * D;
+        oracle_rope_apply_vec(x + off, cos_t + s * (D / 2), sin_t + s * (D / 2),
+                              D, y + off);
+      }
+}
+
+/* ---- attention, step 3 ------------------------------------------------- */
+
+typedef struct {
+  const double *q, *k, *v, *cos_t, *sin_t;
+  int B, H, D;
+  int64_t S;
+  const int64_t *rows; /* query token indices to evaluate */
+  int64_t n_rows;
+  double *out; /* [B, n_rows, H, D] */
+  int64_t next_unit; /* shared work counter over (b, h) */
+  pthread_mutex_t lock;
+} attn_job;
+
+/* One (batch, head) pair: rotate every key of that head, then evaluate each
+ * requested query row straight from the definition. */
+static void attn_unit(attn_job *J, int b, int h) {
+  const int D = J->D, H = J->H;
+  const int64_t S = J->S;
+  const double scale = 1.0 / sqrt((double)D);
+  double *khat = (double *)malloc(sizeof(double) * (size_t)S * D);
+  double *z = (double *)malloc(sizeof(double) * (size_t)S);
+  double *qhat = (double *)malloc(sizeof(double) * (size_t)D);
+  for (int64_t j = 0; j < S; ++j) {
+    int64_t off = (((int64_t)b * S + j) * H + h) * D;
+    oracle_rope_apply_vec(J->k + off, J->cos_t + j * (D / 2),
+                          J->sin_t + j * (D / 2), D, khat + j * D);
+  }
+  for (int64_t r = 0; r < J->n_rows; ++r) {
+    int64_t i = J->rows[r];
+    int64_t qoff = (((int64_t)b * S + i) * H + h) * D;
+    oracle_rope_apply_vec(J->q + qoff, J->cos_t + i * (D / 2),
+                          J->sin_t + i * (D / 2), D, qhat);
+    /* logits z_j = q^_i . k^_j / sqrt(D) */
+    double zmax = -INFINITY;
+    for (int64_t j = 0; j < S; ++j) {
+      double acc = 0.0;
+      for (int c = 0; c < D; ++c) acc += qhat[c] * khat[j * D + c];
+      z[j] = acc * scale;
+      if (z[j] > zmax) zmax = z[j];
+    }
+    /* softmax over all keys (the max is subtracted only to keep exp finite;
+     * it cancels in the ratio), then the weighted sum of V */
+    double denom = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      z[j] = exp(z[j] - zmax);
+      denom += z[j];
+    }
+    double *o = J->out + (((int64_t)b * J->n_rows + r) * H + h) * D;
+    for (int c = 0; c < D; ++c) o[c] = 0.0;
+    for (int64_t j = 0; j < S; ++j) {
+      const double *vj = J->v + (((int64_t)b * S + j) * H + h) * D;
+      double w = z[j] / denom;
+      for (int c = 0; c < D; ++c) o[c] += w * vj[c];
+    }
+  }
+  free(khat);
+  free(z);
+  free(qhat);
+}
+
+static void *attn_worker(void *arg) {
+  attn_job *J = (attn_job *)arg;
+  for (;;) {
+    pthread_mutex_lock(&J->lock);
+    int64_t u = J->next_unit++;
+    pthread_mutex_unlock(&J->lock);
+    if (u >= (int64_t)J->B * J->H) break;
+    attn_unit(J, (int)(u / J->H), (int)(u % J->H));
+  }
+  return NULL;
+}
+
+/* Joint RoPE attention for the query tokens listed in rows[0..n_rows) (every
+ * token when rows is NULL), all batch elements and heads. ids = [txt ; img]
+ * already concatenated, [S, n_axes]. out is [B, n_rows, H, D]. Work over
+ * (b, h) is spread on n_threads POSIX threads; the arithmetic of each output
+ * does not depend on the thread count. Returns 0, or -1 on bad arguments. */
+int oracle_joint_rope_attention(const double *q, const double *k,
+                                const double *v, int B, int64_t S, int H, int D,
+                                const int32_t *ids, const int32_t *axes_dims,
+                                int n_axes, double theta, const int64_t *rows,
+                                int64_t n_rows, int n_threads, double *out) {
+  int sum = 0;
+  for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
+  if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0) return -1;
+  double *cos_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  double *sin_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  int64_t *all_rows = NULL;
+  if (oracle_rope_tables(ids, S, axes_dims, n_axes, theta, cos_t, sin_t) != 0) {
+    free(cos_t);
+    free(sin_t);
+    return -1;
+  }
+  if (rows == NULL) {
+    all_rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)S);
+    for (int64_t i = 0; i < S; ++i) all_rows[i] = i;
+    rows = all_rows;
+    n_rows = S;
+  }
+  attn_job J;
+  J.q = q; J.k = k; J.v = v; J.cos_t = cos_t; J.sin_t = sin_t;
+  J.B = B; J.H = H; J.D = D; J.S = S;
+  J.rows = rows; J.n_rows = n_rows; J.out = out; J.next_unit = 0;
+  pthread_mutex_init(&J.lock, NULL);
+  if (n_threads < 1) n_threads = 1;
+  pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
+  for (int t = 0; t < n_threads; ++t) pthread_create(&th[t], NULL, attn_worker, &J);
+  for (int t = 0; t < n_threads; ++t) pthread_join(th[t], NULL);
+  pthread_mutex_destroy(&J.lock);
+  free(th);
+  free(all_rows);
+  free(cos_t);
+  free(sin_t);
+  return 0;
+}

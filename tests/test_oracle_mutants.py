@@ -1,0 +1,79 @@
+"""Plant plausible mistakes in a copy of the oracle and require the pins to see them.
+
+Each mutant is the oracle's own C source with one textual change, compiled
+into a temporary library on the CPU. A mutant that passes every pin would
+mean the pins cannot tell that mistake from the method.
+"""
+import os
+
+import pytest
+
+import oracle
+from tests import oracle_checks as oc
+
+MUTANTS = {
+    # frequencies over the whole head width instead of each axis' width
+    "freq_full_width": ("pow(theta, -2.0 * (double)j / (double)d_a)",
+                        "pow(theta, -2.0 * (double)j / 128.0)"),
+    # exponent missing the factor 2
+    "freq_no_two": ("pow(theta, -2.0 * (double)j / (double)d_a)",
+                    "pow(theta, -1.0 * (double)j / (double)d_a)"),
+    # axes read in reverse column order
+    "axis_order": ("(double)ids[s * n_axes + a]", "(double)ids[s * n_axes + (n_axes - 1 - a)]"),
+    # wrong sign in the rotation
+    "rotation_sign": ("y[2 * p] = re * c[p] - im * sn[p];",
+                      "y[2 * p] = re * c[p] + im * sn[p];"),
+    # rotation by the inverse angle
+    "rotation_inverse": ("y[2 * p + 1] = re * sn[p] + im * c[p];",
+                         "y[2 * p + 1] = -re * sn[p] + im * c[p];"),
+    # split-halves pairing instead of adjacent pairs
+    "split_halves": ("double re = x[2 * p], im = x[2 * p + 1];",
+                     "double re = x[p], im = x[p + D / 2];"),
+    # no 1/sqrt(D) scale
+    "no_scale": ("z[j] = acc * scale;", "z[j] = acc;"),
+    # softmax not normalised
+    "no_normalise": ("double w = z[j] / denom;", "double w = z[j];"),
+    # queries left unrotated
+    "q_unrotated": ("J->sin_t + i * (D / 2), D, qhat);",
+                    "J->sin_t + i * (D / 2), D, qhat); for (int c = 0; c < D; ++c) "
+                    "qhat[c] = J->q[qoff + c];"),
+    # keys rotated with the query's position
+    "k_wrong_position": ("J->cos_t + j * (D / 2),\n                          J->sin_t + j * (D / 2)",
+                         "J->cos_t + 0 * (D / 2),\n                          J->sin_t + 0 * (D / 2)"),
+    # values read from the key tensor
+    "v_from_k": ("const double *vj = J->v +", "const double *vj = J->k +"),
+    # off-by-one in the key loop
+    "skip_last_key": ("for (int64_t j = 0; j < S; ++j) {\n      double acc",
+                      "for (int64_t j = 0; j < S - 1; ++j) {\n      double acc"),
+}
+
+
+def _run_checks(orc):
+    failed = []
+    for check in oc.ALL_CHECKS:
+        try:
+            check(orc)
+        except AssertionError:
+            failed.append(check.__name__)
+        except ImportError:
+            pass
+    return failed
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    pytest.importorskip("mpmath")
+    src = open(oracle.SOURCE).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation anchor not found once: {old!r}"
+    mpath = tmp_path / f"mutant_{name}.c"
+    mpath.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(mpath), str(tmp_path / f"libmutant_{name}.so"))
+    failed = _run_checks(oracle.Oracle(lib))
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_unmutated_source_passes(tmp_path):
+    pytest.importorskip("mpmath")
+    lib = oracle.compile_source(oracle.SOURCE, str(tmp_path / "libclean.so"))
+    assert _run_checks(oracle.Oracle(lib)) == []
