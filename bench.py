@@ -1,0 +1,438 @@
+"""Bench: joint RoPE attention TFLOP/s on the klein-9B 1024^2 shape.
+
+One step is one pass of the whole hot path over one batch: the RoPE table
+kernel for the joint ids, then the attention kernel (RoPE fused into the
+Q/K tile loads, QK^T and PV on tcgen05, online softmax). FLOPs per step are
+4 * B * H * S^2 * 128.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload klein9b]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun, one rank per GPU) every
+rank runs the same-shaped workload on its own seeded inputs with no data
+exchange (heads and batches are independent): weak scaling, and `value` is
+all ranks' FLOPs over the slowest rank's time.
+
+`--impl reference` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of query rows of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "joint RoPE-attention bf16 TFLOP/s at klein-9B 1024² shape; % dense-BF16 peak"
+UNIT = "TFLOP/s"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attention_klein9b_ncu.txt")
+KERNEL_SOURCE = os.path.join(ROOT, "diffusion_transformer_joint_gb300", "csrc",
+                             "attention_sm103a.cu")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _kernel_hash():
+    with open(KERNEL_SOURCE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _profiled_traffic():
+    """dram bytes per attention launch from the committed ncu summary, when
+    it was taken on the current kernel source; else None."""
+    try:
+        vals = {}
+        for line in open(PROFILE_SUMMARY):
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+        if vals.get("kernel_source_sha256_16") != _kernel_hash():
+            return None
+        return float(vals["dram_bytes_per_launch_klein9b"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"flux_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ ours
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    from diffusion_transformer_joint_gb300 import binding
+    from diffusion_transformer_joint_gb300 import build as cuda_build
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(cuda_build.LIB_PATH):
+        cuda_build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+
+    w = W.WORKLOADS[args.workload]
+    txt_np, img_np = W.workload_ids(w)
+    import numpy as np
+
+    ids = torch.from_numpy(np.concatenate([txt_np, img_np])).to(dev)
+    set_bytes = 3 * w.B * w.S * w.H * w.D * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    sets = []
+    for i in range(n_sets):
+        q, k, v = W.workload_qkv(w, seed_offset=100000 * rank + 17 * i)
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
+    P = w.D // 2
+    cos_t = torch.empty((w.S, P), dtype=torch.float32, device=dev)
+    sin_t = torch.empty((w.S, P), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i, ev_mid=None):
+        q, k, v, out = sets[i % n_sets]
+        binding.rope_tables(ids, cos_out=cos_t, sin_out=sin_t, stream=stream)
+        if ev_mid is not None:
+            ev_mid.record(stream)
+        binding.joint_rope_attention_tabled(q, k, v, cos_t, sin_t, status, out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+
+    K = args.steps
+    ev_start = torch.cuda.Event(enable_timing=True)
+    ev_end = torch.cuda.Event(enable_timing=True)
+    ev_mid = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_after = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            ev_start.record(stream)
+            for i in range(K):
+                step(i, ev_mid[i])
+                ev_after[i].record(stream)
+            ev_end.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    total_ms = ev_start.elapsed_time(ev_end)
+    attn_ms = [ev_mid[i].elapsed_time(ev_after[i]) for i in range(K)]
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed steps")
+
+    t_max = total_ms
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+
+    # end-to-end through the public one-call API with host buffers
+    e2e = run_e2e(w, dev, K, args.warmup, binding, W, torch, np, txt_np, img_np)
+    if dist is not None:
+        e = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(e, op=dist.ReduceOp.MAX)
+        e2e["ms_per_step"] = float(e.item())
+
+    if rank != 0:
+        return None
+    peaks, peak_src = _peaks()
+    flops_step = w.flops
+    value = world * flops_step * K / (t_max * 1e-3) / 1e12
+    attn_avg_ms = statistics.mean(attn_ms)
+    achieved = flops_step / (attn_avg_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = _profiled_traffic()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_max / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, FLUX.2 (T,H,W,L) ids)",
+        "config": {
+            "workload": f"{w.name}: B={w.B} H={w.H} S={w.S} ({w.S_txt} text + {w.S_img} image) "
+                        f"head_dim={w.D} axes=(32,32,32,32) theta=2000 non-causal",
+            "B": w.B, "H": w.H, "S": w.S, "S_txt": w.S_txt, "S_img": w.S_img, "head_dim": w.D,
+            "parallelism": f"replicas x{world} (heads/batches independent, no collective)",
+            "l2": f"inputs rotate over {n_sets} sets of {set_bytes / 2**20:.0f} MiB "
+                  f"({n_sets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
+            "step": "rope_tables kernel + attention kernel (tables rebuilt every step)",
+        },
+        "pct_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {
+            "bound": "tensor",
+            "kernel": "joint_rope_attention_kernel",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "TFLOP/s",
+            "frac": round(achieved / peak, 4),
+            "frac_of_sustained": round(achieved / peak_sus, 4),
+            "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "traffic": traffic,
+            "algorithmic_flops_per_launch": flops_step,
+            "algorithmic_bytes_per_launch": w.io_bytes,
+            "avg_launch_ms": round(attn_avg_ms, 4),
+        },
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(world * flops_step / (e2e["ms_per_step"] * 1e-3) / 1e12, 2),
+                "unit": UNIT, "ms_per_step": round(e2e["ms_per_step"], 4),
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                "api": "flux_joint_rope_attention (one call: tables + attention)"},
+        "gpu_launches": 2 * K,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
+    return line
+
+
+def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
+    """Same metric through the one-call API: pinned host inputs are copied in,
+    the call runs, the output is copied back, every step inside the timing."""
+    q, k, v = W.workload_qkv(w, seed_offset=555)
+    hq, hk, hv = (t.pin_memory() for t in (q, k, v))
+    htxt = torch.from_numpy(txt_np).pin_memory()
+    himg = torch.from_numpy(img_np).pin_memory()
+    hout = torch.empty_like(hq).pin_memory()
+    dq, dk, dv = (torch.empty_like(t, device=dev) for t in (q, k, v))
+    dtxt = torch.empty_like(htxt, device=dev)
+    dimg = torch.empty_like(himg, device=dev)
+    dout = torch.empty_like(dq)
+    ws = torch.zeros(binding.workspace_bytes(w.S), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def one():
+        for d, h in ((dq, hq), (dk, hk), (dv, hv), (dtxt, htxt), (dimg, himg)):
+            d.copy_(h, non_blocking=True)
+        binding.joint_rope_attention(dq, dk, dv, dtxt, dimg, out=dout, workspace=ws,
+                                     stream=stream)
+        hout.copy_(dout, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, warmup)):
+            one()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            one()
+        e1.record(stream)
+    stream.synchronize()
+    if binding.query_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, htxt, himg))
+    d2h = hout.numel() * hout.element_size()
+    return {"ms_per_step": e0.elapsed_time(e1) / K, "h2d": h2d, "d2h": d2h}
+
+
+# --------------------------------------------------------- CPU baseline
+
+
+def _oracle_sample(w, rows, threads, q, k, v, txt, img):
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.joint_rope_attention(q, k, v, txt, img, rows=rows, threads=threads)
+    return time.perf_counter() - t0
+
+
+def _oracle_inputs(w):
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    q, k, v = W.workload_qkv(w)
+    txt, img = W.workload_ids(w)
+    return q.float().numpy(), k.float().numpy(), v.float().numpy(), txt, img
+
+
+def _rows_for(w, seconds, threads, inputs):
+    import numpy as np
+
+    probe = np.arange(0, w.S, max(1, w.S // 16), dtype=np.int64)[:16]
+    t = _oracle_sample(w, probe, threads, *inputs)
+    per_row = t / probe.size
+    n = int(max(16, min(w.S, seconds / max(per_row, 1e-9))))
+    return np.linspace(0, w.S - 1, n).astype(np.int64)
+
+
+def cpu_baseline(w, target_s=12.0):
+    """The oracle as it stands, timed on the host cores on a bounded sample of
+    query rows (all batch elements and heads of each row) of the workload."""
+    import oracle
+
+    threads = oracle.default_threads()
+    inputs = _oracle_inputs(w)
+    rows = _rows_for(w, target_s, threads, inputs)
+    t = _oracle_sample(w, rows, threads, *inputs)
+    flops = 4 * w.B * w.H * rows.size * w.S * w.D
+    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "sample": f"{rows.size} of {w.S} query rows x all {w.B * w.H} (batch, head) pairs of "
+                      f"{w.name} against all {w.S} keys, fp64, {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores: each step is a bounded sample of the same
+    workload; the line carries the same metric and unit as ours."""
+    if rank != 0:
+        return None
+    import oracle
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    oracle.build()
+    w = W.WORKLOADS[args.workload]
+    threads = oracle.default_threads()
+    inputs = _oracle_inputs(w)
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    rows = _rows_for(w, min(4.0, budget_s), threads, inputs)
+    for _ in range(args.warmup):
+        _oracle_sample(w, rows[:8], threads, *inputs)
+    times = [_oracle_sample(w, rows, threads, *inputs) for _ in range(args.steps)]
+    flops = 4 * w.B * w.H * rows.size * w.S * w.D
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    sample = (f"{rows.size} of {w.S} query rows x all {w.B * w.H} (batch, head) pairs of "
+              f"{w.name} per step, fp64")
+    return {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, FLUX.2 (T,H,W,L) ids)",
+        "config": {"workload": f"{w.name}: B={w.B} H={w.H} S={w.S} ({w.S_txt} text + "
+                               f"{w.S_img} image) head_dim={w.D} axes=(32,32,32,32) theta=2000 "
+                               "non-causal", "B": w.B, "H": w.H, "S": w.S},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default="klein9b")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        line = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

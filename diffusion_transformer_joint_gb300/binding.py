@@ -1,0 +1,186 @@
+"""Python binding of libflux_attn.so (the C-ABI in include/flux_attn.h).
+
+Argument marshalling only: torch supplies device memory and streams, every
+step of the computation runs in the library's kernels. There is no fallback:
+a missing library, a CPU tensor or a non-zero status raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+AXES_DIMS = (32, 32, 32, 32)
+THETA = 2000.0
+
+STATUS = {
+    0: "FLUX_OK", -1: "FLUX_ERR_NULL", -2: "FLUX_ERR_SHAPE", -3: "FLUX_ERR_AXES",
+    -4: "FLUX_ERR_ALIGN", -5: "FLUX_ERR_WORKSPACE", -6: "FLUX_ERR_CUDA",
+    -7: "FLUX_ERR_DEVICE_TIMEOUT", -8: "FLUX_ERR_UNSUPPORTED", -9: "FLUX_ERR_ALIAS",
+}
+
+# every symbol include/flux_attn.h declares
+EXPORTS = ("flux_rope_tables", "flux_joint_rope_attention_workspace",
+           "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
+           "flux_query_status", "flux_status_string")
+
+
+class FluxError(RuntimeError):
+    def __init__(self, fn: str, status: int, lib=None):
+        msg = lib.flux_status_string(status).decode() if lib is not None else ""
+        super().__init__(f"{fn}: {STATUS.get(status, status)} ({msg})")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.environ.get("FLUX_ATTN_LIB", _build.LIB_PATH)
+
+
+def load(path: str | None = None):
+    """Load (once) and return the ctypes handle; raises if the library is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or library_path()
+            if not os.path.exists(p):
+                raise RuntimeError(f"CUDA library not built: {p} (run "
+                                   "python -m diffusion_transformer_joint_gb300.build)")
+            lib = ctypes.CDLL(p)
+            V, I64, I32, SZ, D = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
+                                  ctypes.c_size_t, ctypes.c_double)
+            lib.flux_rope_tables.argtypes = [V, I64, V, I32, D, V, V, V]
+            lib.flux_rope_tables.restype = I32
+            lib.flux_joint_rope_attention_workspace.argtypes = [I64, I32]
+            lib.flux_joint_rope_attention_workspace.restype = SZ
+            lib.flux_joint_rope_attention.argtypes = [V, V, V, V, I64, V, I64, I32, I32, I32,
+                                                      V, I32, D, V, V, SZ, V]
+            lib.flux_joint_rope_attention.restype = I32
+            lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, V, I32, I64, I32, I32,
+                                                             V, V, V]
+            lib.flux_joint_rope_attention_tabled.restype = I32
+            lib.flux_query_status.argtypes = [V, V]
+            lib.flux_query_status.restype = I32
+            lib.flux_status_string.argtypes = [I32]
+            lib.flux_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _axes_array(axes_dims):
+    arr = (ctypes.c_int32 * len(axes_dims))(*[int(a) for a in axes_dims])
+    return arr, len(axes_dims)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None and t.numel() > 0 else None
+
+
+def _stream_handle(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need_cuda(name, t, dtype):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (no CPU path exists)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def workspace_bytes(S: int, D: int = 128) -> int:
+    return int(load().flux_joint_rope_attention_workspace(int(S), int(D)))
+
+
+def rope_tables(ids, axes_dims=AXES_DIMS, theta=THETA, cos_out=None, sin_out=None, stream=None):
+    """fp32 cos, sin [S, sum(axes_dims)/2] for int32 ids [S, n_axes] on the GPU."""
+    import torch
+
+    lib = load()
+    _need_cuda("ids", ids, torch.int32)
+    S, n_axes = ids.shape
+    P = sum(int(a) for a in axes_dims) // 2
+    if cos_out is None:
+        cos_out = torch.empty((S, P), dtype=torch.float32, device=ids.device)
+    if sin_out is None:
+        sin_out = torch.empty((S, P), dtype=torch.float32, device=ids.device)
+    axes, n = _axes_array(axes_dims)
+    if n != n_axes:
+        raise ValueError("ids' last dimension must equal len(axes_dims)")
+    rc = lib.flux_rope_tables(_ptr(ids), S, axes, n, float(theta), _ptr(cos_out), _ptr(sin_out),
+                              _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_rope_tables", rc, lib)
+    return cos_out, sin_out
+
+
+def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA, out=None,
+                         workspace=None, stream=None):
+    """softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v over the joint sequence [txt ; img].
+
+    q, k, v: bf16 CUDA [B, S, H, 128]; txt_ids [S_txt, n_axes], img_ids
+    [S_img, n_axes] int32 CUDA (either may be None / empty). Returns ``out``.
+    """
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+    B, S, H, D = q.shape
+    S_txt = 0 if txt_ids is None else int(txt_ids.shape[0])
+    S_img = 0 if img_ids is None else int(img_ids.shape[0])
+    for name, t in (("txt_ids", txt_ids), ("img_ids", img_ids)):
+        if t is not None and t.numel() > 0:
+            _need_cuda(name, t, torch.int32)
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+    if workspace is None:
+        workspace = torch.empty(max(workspace_bytes(max(S, 1), D), 256), dtype=torch.uint8,
+                                device=q.device)
+    axes, n = _axes_array(axes_dims)
+    rc = lib.flux_joint_rope_attention(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes, n,
+        float(theta), _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention", rc, lib)
+    return out
+
+
+def joint_rope_attention_tabled(q, k, v, cos_t, sin_t, status, out=None, stream=None):
+    """Attention with caller-built RoPE tables (see rope_tables); ``status`` is a
+    device int32 tensor of one element that the caller clears."""
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+    _need_cuda("cos_t", cos_t, torch.float32)
+    _need_cuda("sin_t", sin_t, torch.float32)
+    _need_cuda("status", status, torch.int32)
+    B, S, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(cos_t),
+                                              _ptr(sin_t), B, S, H, D, _ptr(out), _ptr(status),
+                                              _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention_tabled", rc, lib)
+    return out
+
+
+def query_status(workspace, stream=None) -> int:
+    """Synchronise and return the device status word of a call's workspace."""
+    lib = load()
+    return int(lib.flux_query_status(_ptr(workspace), _stream_handle(stream)))

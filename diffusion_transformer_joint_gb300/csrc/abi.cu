@@ -1,0 +1,154 @@
+// C-ABI entry points declared in include/flux_attn.h: argument checks, the
+// workspace layout, and the two launches (RoPE tables, then attention).
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "flux_internal.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+// sm_103 check, cached per device ordinal.
+int check_device() {
+  static int cached[64];  // 0 unknown, 1 ok, -1 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLUX_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return FLUX_ERR_UNSUPPORTED;
+  if (cached[dev] == 0) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return FLUX_ERR_CUDA;
+    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+  }
+  return cached[dev] == 1 ? FLUX_OK : FLUX_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *flux_status_string(int status) {
+  switch (status) {
+    case FLUX_OK: return "ok";
+    case FLUX_ERR_NULL: return "a required pointer is NULL";
+    case FLUX_ERR_SHAPE: return "B, H, S or D out of the supported range";
+    case FLUX_ERR_AXES: return "axes_dims must be positive, even, sum to D; 1 <= n_axes <= 8";
+    case FLUX_ERR_ALIGN: return "q, k, v and out must be 16-byte aligned";
+    case FLUX_ERR_WORKSPACE: return "workspace NULL, not 256-byte aligned, or too small";
+    case FLUX_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+    case FLUX_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device timeout)";
+    case FLUX_ERR_UNSUPPORTED: return "the current device is not sm_103 (GB300)";
+    case FLUX_ERR_ALIAS: return "out overlaps q, k or v";
+    default: return "unknown status";
+  }
+}
+
+int flux_rope_tables(const int32_t *ids, int64_t S, const int32_t *axes_dims, int n_axes,
+                     double theta, float *cos_out, float *sin_out, void *stream) {
+  if (ids == nullptr || cos_out == nullptr || sin_out == nullptr || axes_dims == nullptr)
+    return FLUX_ERR_NULL;
+  if (S < 1 || S > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+  const cudaError_t e = flux::launch_rope_tables(ids, S, nullptr, 0, pp, cos_out, sin_out,
+                                                 static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FLUX_OK : FLUX_ERR_CUDA;
+}
+
+size_t flux_joint_rope_attention_workspace(int64_t S, int D) {
+  if (S < 1 || S > 0x7FFFFFFFLL || D <= 0 || (D & 1)) return 0;
+  return flux::kStatusBytes + 2 * flux::table_bytes(S, D);
+}
+
+int flux_joint_rope_attention(const void *q, const void *k, const void *v,
+                              const int32_t *txt_ids, int64_t S_txt, const int32_t *img_ids,
+                              int64_t S_img, int B, int H, int D, const int32_t *axes_dims,
+                              int n_axes, double theta, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
+    return FLUX_ERR_NULL;
+  if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr)) return FLUX_ERR_NULL;
+  if (S_txt < 0 || S_img < 0) return FLUX_ERR_SHAPE;
+  const int64_t S = S_txt + S_img;
+  if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
+    return FLUX_ERR_SHAPE;
+  if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  if (2 * pp.n_pairs != D) return FLUX_ERR_AXES;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FLUX_ERR_ALIGN;
+  const size_t tensor_bytes = static_cast<size_t>(B) * static_cast<size_t>(S) *
+                              static_cast<size_t>(H) * static_cast<size_t>(D) * 2;
+  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
+      overlaps(out, tensor_bytes, v, tensor_bytes))
+    return FLUX_ERR_ALIAS;
+  const size_t need = flux_joint_rope_attention_workspace(S, D);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < need)
+    return FLUX_ERR_WORKSPACE;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  float *cos_t = reinterpret_cast<float *>(ws + flux::kStatusBytes);
+  float *sin_t = reinterpret_cast<float *>(ws + flux::kStatusBytes + flux::table_bytes(S, D));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
+  if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, cos_t, sin_t, st) !=
+      cudaSuccess)
+    return FLUX_ERR_CUDA;
+  if (flux::launch_joint_attention(q, k, v, out, cos_t, sin_t, status, B, S, H, st) !=
+      cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return FLUX_OK;
+}
+
+int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
+                                     const float *cos_t, const float *sin_t, int B, int64_t S,
+                                     int H, int D, void *out, int32_t *status, void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cos_t == nullptr ||
+      sin_t == nullptr || status == nullptr)
+    return FLUX_ERR_NULL;
+  if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
+    return FLUX_ERR_SHAPE;
+  if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(cos_t) ||
+      !aligned16(sin_t))
+    return FLUX_ERR_ALIGN;
+  const size_t tensor_bytes = static_cast<size_t>(B) * static_cast<size_t>(S) *
+                              static_cast<size_t>(H) * static_cast<size_t>(D) * 2;
+  if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
+      overlaps(out, tensor_bytes, v, tensor_bytes))
+    return FLUX_ERR_ALIAS;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+  if (flux::launch_joint_attention(q, k, v, out, cos_t, sin_t, status, B, S, H,
+                                   static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return FLUX_OK;
+}
+
+int flux_query_status(const void *workspace, void *stream) {
+  if (workspace == nullptr) return FLUX_ERR_NULL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FLUX_ERR_CUDA;
+  int status = 0;
+  if (cudaMemcpy(&status, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return status;
+}
+
+}  // extern "C"

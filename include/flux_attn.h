@@ -1,0 +1,163 @@
+/*
+ * flux_attn.h: C-ABI of the GB300 (sm_103a) joint RoPE attention library.
+ *
+ * The operation is the attention core of the FLUX.2 MMDiT denoiser: the text
+ * and image (plus reference-image) tokens form one joint sequence, queries
+ * and keys are rotated by a 4-axis N-D RoPE built from per-token (T, H, W, L)
+ * position ids, and every token attends to every token.
+ *
+ * Sources for the definition:
+ *   - "Diffusers 中 Flux2Transformer2DModel 全面解析", sections
+ *     "模型配置参数全解" (attention_head_dim 128, axes_dims_rope (32,32,32,32),
+ *     rope_theta 2000), "前向传播输入输出约定" (4-d position ids whose last
+ *     dimension equals the number of axes; one id set shared by the batch;
+ *     each axis gets its own 1-D RoPE and the axes are concatenated) and
+ *     "内部架构双流块与单流块" (text and image streams concatenated for one
+ *     joint attention).
+ *   - "FLUX.2 [klein]" survey page, section "模型架构" (axes_dim always
+ *     [32,32,32,32], theta 2000; N-D RoPE (EmbedND); reference-image tokens
+ *     concatenated with the noisy tokens).
+ *   - "Transformer架构解析FLUX.2-klein-base-9b-nvfp4", section 2
+ *     "核心引擎自注意力机制如何工作" (scaled dot-product attention:
+ *     softmax(Q K^T / sqrt(d_k)) V with d_k the head size).
+ *
+ * Conventions shared by every entry point:
+ *   - Device pointers refer to memory on the CUDA device that is current on
+ *     the calling thread; the caller owns every buffer, and the library
+ *     allocates nothing and frees nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued asynchronously; nothing synchronises.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns a negative flux_status and enqueues nothing. A launch
+ *     failure returns FLUX_ERR_CUDA.
+ *   - Device-side failures (a bounded wait inside a kernel that ran out)
+ *     never trap: the kernel records FLUX_ERR_DEVICE_TIMEOUT in the status
+ *     word inside the caller's workspace and returns; read it with
+ *     flux_query_status().
+ */
+#ifndef FLUX_ATTN_H
+#define FLUX_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FLUX_OK = 0,
+  FLUX_ERR_NULL = -1,           /* a required pointer is NULL */
+  FLUX_ERR_SHAPE = -2,          /* B, H, S or D out of the supported range */
+  FLUX_ERR_AXES = -3,           /* axes_dims not even / not summing to D / n_axes out of range */
+  FLUX_ERR_ALIGN = -4,          /* a pointer is not 16-byte aligned */
+  FLUX_ERR_WORKSPACE = -5,      /* workspace NULL, misaligned (256 B) or too small */
+  FLUX_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
+  FLUX_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see flux_query_status) */
+  FLUX_ERR_UNSUPPORTED = -8,    /* the current device is not sm_103 */
+  FLUX_ERR_ALIAS = -9           /* out overlaps q, k or v */
+} flux_status;
+
+/* Largest number of RoPE axes accepted (FLUX.2 uses 4). */
+#define FLUX_MAX_AXES 8
+
+/*
+ * flux_rope_tables: cos/sin tables of the N-D RoPE.
+ *
+ * For token s and rotation pair p (channels 2p and 2p+1 of a head), with p in
+ * axis a's block [o_a, o_a + axes_dims[a]/2), o_a = sum_{a'<a} axes_dims[a']/2,
+ * and j = p - o_a:
+ *     angle(s, p) = ids[s, a] * theta^(-2 j / axes_dims[a])
+ *     cos_out[s, p] = cos(angle),  sin_out[s, p] = sin(angle)
+ * The angle is formed in double precision and reduced to [-pi, pi] before the
+ * fp32 cosine and sine, so any int32 id value is accurate to ~2e-7.
+ *
+ *   ids        device, int32 [S, n_axes] row-major (one row per token).
+ *   S          number of tokens, 1 <= S <= 2^31 - 1.
+ *   axes_dims  HOST, int32 [n_axes]; each entry positive and even, the sum
+ *              P2 = sum(axes_dims) at most 512.
+ *   n_axes     1 .. FLUX_MAX_AXES.
+ *   theta      frequency base, > 0 (2000 for FLUX.2).
+ *   cos_out, sin_out  device, fp32 [S, P2/2] row-major; written, not read.
+ *   stream     cudaStream_t as void*.
+ * Returns FLUX_OK or a negative flux_status.
+ */
+int flux_rope_tables(const int32_t *ids, int64_t S, const int32_t *axes_dims, int n_axes,
+                     double theta, float *cos_out, float *sin_out, void *stream);
+
+/*
+ * flux_joint_rope_attention_workspace: bytes of device workspace that
+ * flux_joint_rope_attention needs for a joint sequence of S tokens and head
+ * width D (the RoPE tables, 2 * S * (D/2) fp32, plus a 256-byte status
+ * block). Returns 0 when S < 1 or D is not positive and even.
+ */
+size_t flux_joint_rope_attention_workspace(int64_t S, int D);
+
+/*
+ * flux_joint_rope_attention: out = softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v
+ * over the joint token sequence [txt ; img], non-causal, per batch element
+ * and head.
+ *
+ *   q, k, v    device, bf16 [B, S, H, D] row-major (D fastest), S = S_txt + S_img,
+ *              text tokens first. 16-byte aligned.
+ *   txt_ids    device, int32 [S_txt, n_axes]; may be NULL when S_txt == 0.
+ *   img_ids    device, int32 [S_img, n_axes]; may be NULL when S_img == 0.
+ *              The same ids apply to every batch element.
+ *   B, H       batch and heads, >= 1, B * H * ceil(S/128) < 2^31.
+ *   D          head width; must be 128.
+ *   axes_dims  HOST, int32 [n_axes], even entries summing to D.
+ *   theta      RoPE frequency base (2000 for FLUX.2).
+ *   out        device, bf16 [B, S, H, D], 16-byte aligned, must not overlap q/k/v.
+ *   workspace  device, >= flux_joint_rope_attention_workspace(S, D) bytes,
+ *              256-byte aligned, owned by the caller and not shared by calls
+ *              in flight at the same time. Its status word is cleared by each
+ *              call before the attention kernel runs.
+ *   stream     cudaStream_t as void*.
+ *
+ * Numerics: bf16 inputs, RoPE applied in fp32 and rounded to bf16 for the
+ * tensor-core products, fp32 accumulation and softmax, bf16 output rounded
+ * to nearest even.
+ *
+ * Returns FLUX_OK when both kernels were enqueued, else a negative status.
+ * Requires an sm_103 device (GB300).
+ */
+int flux_joint_rope_attention(const void *q, const void *k, const void *v,
+                              const int32_t *txt_ids, int64_t S_txt,
+                              const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                              const int32_t *axes_dims, int n_axes, double theta, void *out,
+                              void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * flux_joint_rope_attention_tabled: the same attention, with the RoPE tables
+ * supplied by the caller (built once by flux_rope_tables for the joint id
+ * sequence and reused, e.g. by every attention layer of one denoiser step:
+ * the position ids do not change between layers).
+ *
+ *   q, k, v, out  as for flux_joint_rope_attention, [B, S, H, D], D == 128.
+ *   cos_t, sin_t  device, fp32 [S, D/2] as written by flux_rope_tables; 16-byte
+ *                 aligned.
+ *   status        device int32 word; the kernel writes FLUX_ERR_DEVICE_TIMEOUT
+ *                 there if a bounded wait runs out and never writes it
+ *                 otherwise (the caller clears it).
+ *   stream        cudaStream_t as void*.
+ * Returns FLUX_OK when the kernel was enqueued, else a negative status.
+ */
+int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
+                                     const float *cos_t, const float *sin_t, int B, int64_t S,
+                                     int H, int D, void *out, int32_t *status, void *stream);
+
+/*
+ * flux_query_status: synchronises `stream`, reads the device status word of
+ * `workspace` and returns it (FLUX_OK, or FLUX_ERR_DEVICE_TIMEOUT when a
+ * kernel of the last call gave up a bounded wait). FLUX_ERR_CUDA when the
+ * synchronisation or the copy fails.
+ */
+int flux_query_status(const void *workspace, void *stream);
+
+/* flux_status_string: static description of a status code (never NULL). */
+const char *flux_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FLUX_ATTN_H */

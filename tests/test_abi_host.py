@@ -1,0 +1,98 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments with the documented status before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from diffusion_transformer_joint_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def _declared_symbols():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"\b(flux_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_symbols()
+    assert set(binding.EXPORTS) <= set(declared)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in binding.STATUS:
+        assert lib.flux_status_string(code)
+    assert lib.flux_status_string(12345) == b"unknown status"
+
+
+def test_workspace_size(lib):
+    assert lib.flux_joint_rope_attention_workspace(4608, 128) == 256 + 2 * 4608 * 64 * 4
+    assert lib.flux_joint_rope_attention_workspace(80, 128) == 256 + 2 * 20480
+    assert lib.flux_joint_rope_attention_workspace(1, 128) == 256 + 2 * 256
+    assert lib.flux_joint_rope_attention_workspace(0, 128) == 0
+    assert lib.flux_joint_rope_attention_workspace(10, 7) == 0
+
+
+def _call(lib, **kw):
+    args = dict(q=16, k=16 * 1024, v=32 * 1024, txt=None, S_txt=16, img=None, S_img=64, B=1, H=2,
+                D=128, axes=(32, 32, 32, 32), theta=2000.0, out=48 * 1024 * 1024, ws=256 * 4096,
+                ws_bytes=1 << 20)
+    args.update(kw)
+    axes = (ctypes.c_int32 * len(args["axes"]))(*args["axes"])
+    P = lambda x: None if x is None else ctypes.c_void_p(x)
+    txt = args["txt"] if "txt" in kw else 1024
+    img = args["img"] if "img" in kw else 2048
+    return lib.flux_joint_rope_attention(P(args["q"]), P(args["k"]), P(args["v"]), P(txt),
+                                         args["S_txt"], P(img), args["S_img"], args["B"],
+                                         args["H"], args["D"], axes, len(args["axes"]),
+                                         args["theta"], P(args["out"]), P(args["ws"]),
+                                         args["ws_bytes"], None)
+
+
+# Every case fails a host-side check, so no pointer is dereferenced.
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), -1),
+    (dict(out=None), -1),
+    (dict(txt=None), -1),
+    (dict(S_txt=-1), -2),
+    (dict(S_txt=0, S_img=0), -2),
+    (dict(D=64), -2),
+    (dict(B=0), -2),
+    (dict(H=0), -2),
+    (dict(axes=(32, 32, 32)), -3),
+    (dict(axes=(33, 31, 32, 32)), -3),
+    (dict(axes=(32, 32, 32, 32, 0)), -3),
+    (dict(axes=(16,) * 9), -3),
+    (dict(theta=0.0), -3),
+    (dict(q=17), -4),
+    (dict(out=16 + 1024), -9),
+    (dict(ws=None), -5),
+    (dict(ws=256 * 4096 + 16), -5),
+    (dict(ws_bytes=100), -5),
+])
+def test_bad_arguments_rejected_on_host(lib, kw, code):
+    assert _call(lib, **kw) == code
+
+
+def test_rope_tables_bad_arguments(lib):
+    axes = (ctypes.c_int32 * 4)(32, 32, 32, 32)
+    P = ctypes.c_void_p
+    assert lib.flux_rope_tables(None, 4, axes, 4, 2000.0, P(16), P(32), None) == -1
+    assert lib.flux_rope_tables(P(16), 0, axes, 4, 2000.0, P(16), P(32), None) == -2
+    bad = (ctypes.c_int32 * 2)(3, 4)
+    assert lib.flux_rope_tables(P(16), 4, bad, 2, 2000.0, P(16), P(32), None) == -3
