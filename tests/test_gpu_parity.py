@@ -38,7 +38,7 @@ def _run_gpu(q, k, v, txt, img, **kw):
     return out
 
 
-def _compare(gpu_out, q, k, v, txt, img, rows=None, **kw):
+def _compare(gpu_out, q, k, v, txt, img, rows=None, max_abs=MAX_ABS, **kw):
     ref = oracle.joint_rope_attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
                                       txt, img, rows=rows, **kw)
     got = gpu_out.float().cpu().numpy()
@@ -46,7 +46,7 @@ def _compare(gpu_out, q, k, v, txt, img, rows=None, **kw):
         got = got[:, rows]
     err = np.abs(got.astype(np.float64) - ref)
     assert np.isfinite(got).all()
-    assert err.max() <= MAX_ABS, f"max abs err {err.max():.3e}"
+    assert err.max() <= max_abs, f"max abs err {err.max():.3e}"
     assert err.mean() <= MEAN_ABS, f"mean abs err {err.mean():.3e}"
     return err
 
@@ -130,8 +130,11 @@ def test_peaked_softmax_online_rescale():
     logit by ~0.03 (8 * sqrt(2) * 2^-8 / sqrt(3)), which a bf16-operand kernel
     cannot avoid; so the reference here is the oracle's own rotation, rounded
     to bf16 by torch, fed to the oracle's attention with zero ids (identity
-    rotation). What remains is the softmax / rescale / P V path at the
-    standard tolerance.
+    rotation). What remains is the softmax / rescale / P V path. There the
+    bf16 rounding of each softmax weight (unit roundoff u = 2^-9), with the
+    denominator summed from the unrounded fp32 weights, perturbs an output by
+    at most about 2 u max|v| when one weight dominates; the max-abs bound is
+    that plus the standard 1e-2, the mean-abs bound stays 1e-3.
     """
     B, H, S = 1, 2, 517
     q = W.normal_bf16((B, S, H, 128), 45, scale=8.0)
@@ -143,7 +146,8 @@ def test_peaked_softmax_online_rescale():
     qr = torch.from_numpy(oracle.rope_apply(q.double().numpy(), c, s)).to(torch.bfloat16)
     kr = torch.from_numpy(oracle.rope_apply(k.double().numpy(), c, s)).to(torch.bfloat16)
     zero = np.zeros_like(ids)
-    _compare(out, qr, kr, v, zero[:33], zero[33:])
+    bound = MAX_ABS + 2.0 ** -8 * float(v.float().abs().max())
+    _compare(out, qr, kr, v, zero[:33], zero[33:], max_abs=bound)
 
 
 def test_identical_keys_give_mean_of_v():
