@@ -146,6 +146,45 @@ int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v
                                      const float *cos_t, const float *sin_t, int B, int64_t S,
                                      int H, int D, void *out, int32_t *status, void *stream);
 
+/* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
+ * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
+ * on every device that loads this library, held until the process exits. */
+#define FLUX_NOALLOC_MAX_TOKENS 32768
+
+/*
+ * flux_joint_rope_attention_noalloc: flux_joint_rope_attention without a
+ * caller workspace. The pages have no counterpart; it exists for callers that
+ * cannot allocate device memory: a plugin inside a host application whose
+ * allocator owns all device memory and gives plugins none, or code that must
+ * not call cudaMalloc because it can synchronise the device and stall other
+ * streams. The caller still passes inputs and outputs; nothing is allocated
+ * or freed (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * Scratch (RoPE tables and the status word) lives in one fixed file-scope
+ * device array of the library, one per device. Consequences:
+ *   - S_txt + S_img above FLUX_NOALLOC_MAX_TOKENS returns FLUX_ERR_SHAPE and
+ *     launches nothing; D must be 128 as for the regular entry point.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins on the device.
+ *   - Every call shares the one array and it keeps the last call's contents.
+ *     Each call clears the status word and rewrites the tables before the
+ *     attention kernel reads them, so results do not depend on earlier
+ *     calls; but calls that overlap on the GPU (different streams, or
+ *     different host threads, without ordering between them) race on the
+ *     array and give undefined results. Order them on one stream.
+ *   - The device status word is not readable through this entry point; a
+ *     device timeout is not reported (use the regular entry point with
+ *     flux_query_status when that matters).
+ * Arguments, layouts and the other return codes are those of
+ * flux_joint_rope_attention; FLUX_ERR_CUDA also when the address lookup fails.
+ */
+int flux_joint_rope_attention_noalloc(const void *q, const void *k, const void *v,
+                                      const int32_t *txt_ids, int64_t S_txt,
+                                      const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                      const int32_t *axes_dims, int n_axes, double theta,
+                                      void *out, void *stream);
+
 /*
  * flux_query_status: synchronises `stream`, reads the device status word of
  * `workspace` and returns it (FLUX_OK, or FLUX_ERR_DEVICE_TIMEOUT when a
