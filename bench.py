@@ -163,17 +163,16 @@ def run_ours(args, rank, world, local_rank):
         q, k, v = W.workload_qkv(w, seed_offset=100000 * rank + 17 * i)
         sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
     P = w.D // 2
-    cos_t = torch.empty((w.S, P), dtype=torch.float32, device=dev)
-    sin_t = torch.empty((w.S, P), dtype=torch.float32, device=dev)
+    table = torch.empty((w.S, P), dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, ev_mid=None):
         q, k, v, out = sets[i % n_sets]
-        binding.rope_tables(ids, cos_out=cos_t, sin_out=sin_t, stream=stream)
+        binding.rope_tables_packed(ids, out=table, stream=stream)
         if ev_mid is not None:
             ev_mid.record(stream)
-        binding.joint_rope_attention_tabled(q, k, v, cos_t, sin_t, status, out=out, stream=stream)
+        binding.joint_rope_attention_tabled(q, k, v, table, status, out=out, stream=stream)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):

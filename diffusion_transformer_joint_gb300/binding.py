@@ -22,7 +22,7 @@ STATUS = {
 }
 
 # every symbol include/flux_attn.h declares
-EXPORTS = ("flux_rope_tables", "flux_joint_rope_attention_workspace",
+EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_attention_workspace",
            "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
            "flux_query_status", "flux_status_string")
 
@@ -56,13 +56,15 @@ def load(path: str | None = None):
                                   ctypes.c_size_t, ctypes.c_double)
             lib.flux_rope_tables.argtypes = [V, I64, V, I32, D, V, V, V]
             lib.flux_rope_tables.restype = I32
+            lib.flux_rope_tables_packed.argtypes = [V, I64, V, I32, D, V, V]
+            lib.flux_rope_tables_packed.restype = I32
             lib.flux_joint_rope_attention_workspace.argtypes = [I64, I32]
             lib.flux_joint_rope_attention_workspace.restype = SZ
             lib.flux_joint_rope_attention.argtypes = [V, V, V, V, I64, V, I64, I32, I32, I32,
                                                       V, I32, D, V, V, SZ, V]
             lib.flux_joint_rope_attention.restype = I32
-            lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, V, I32, I64, I32, I32,
-                                                             V, V, V]
+            lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, I32, I64, I32, I32, V,
+                                                             V, V]
             lib.flux_joint_rope_attention_tabled.restype = I32
             lib.flux_query_status.argtypes = [V, V]
             lib.flux_query_status.restype = I32
@@ -124,6 +126,36 @@ def rope_tables(ids, axes_dims=AXES_DIMS, theta=THETA, cos_out=None, sin_out=Non
     return cos_out, sin_out
 
 
+def rope_tables_packed(ids, axes_dims=AXES_DIMS, theta=THETA, out=None, stream=None):
+    """Packed table [S, sum(axes_dims)/2] (int32 storage of uint32 words: fp16 cos
+    in bits 0-15, fp16 sin in bits 16-31) for int32 ids [S, n_axes] on the GPU."""
+    import torch
+
+    lib = load()
+    _need_cuda("ids", ids, torch.int32)
+    S, n_axes = ids.shape
+    P = sum(int(a) for a in axes_dims) // 2
+    if out is None:
+        out = torch.empty((S, P), dtype=torch.int32, device=ids.device)
+    axes, n = _axes_array(axes_dims)
+    if n != n_axes:
+        raise ValueError("ids' last dimension must equal len(axes_dims)")
+    rc = lib.flux_rope_tables_packed(_ptr(ids), S, axes, n, float(theta), _ptr(out),
+                                     _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_rope_tables_packed", rc, lib)
+    return out
+
+
+def unpack_table(packed):
+    """(cos, sin) fp32 tensors from a packed table (the fp16 halves, widened)."""
+    import torch
+
+    w = packed.contiguous()
+    halves = w.view(torch.int16).view(torch.float16).reshape(*w.shape, 2)
+    return halves[..., 0].float(), halves[..., 1].float()
+
+
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA, out=None,
                          workspace=None, stream=None):
     """softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v over the joint sequence [txt ; img].
@@ -158,23 +190,21 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
     return out
 
 
-def joint_rope_attention_tabled(q, k, v, cos_t, sin_t, status, out=None, stream=None):
-    """Attention with caller-built RoPE tables (see rope_tables); ``status`` is a
-    device int32 tensor of one element that the caller clears."""
+def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None):
+    """Attention with a caller-built packed table (see rope_tables_packed); ``status``
+    is a device int32 tensor of one element that the caller clears."""
     import torch
 
     lib = load()
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_cuda(name, t, torch.bfloat16)
-    _need_cuda("cos_t", cos_t, torch.float32)
-    _need_cuda("sin_t", sin_t, torch.float32)
+    _need_cuda("table", table, torch.int32)
     _need_cuda("status", status, torch.int32)
     B, S, H, D = q.shape
     if out is None:
         out = torch.empty_like(q)
-    rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(cos_t),
-                                              _ptr(sin_t), B, S, H, D, _ptr(out), _ptr(status),
-                                              _stream_handle(stream))
+    rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H, D,
+                                              _ptr(out), _ptr(status), _stream_handle(stream))
     if rc != 0:
         raise FluxError("flux_joint_rope_attention_tabled", rc, lib)
     return out

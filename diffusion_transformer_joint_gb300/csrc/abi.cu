@@ -61,14 +61,30 @@ int flux_rope_tables(const int32_t *ids, int64_t S, const int32_t *axes_dims, in
   if (rc != FLUX_OK) return rc;
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
-  const cudaError_t e = flux::launch_rope_tables(ids, S, nullptr, 0, pp, cos_out, sin_out,
-                                                 static_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      flux::launch_rope_tables(ids, S, nullptr, 0, pp, flux::TableFormat::kF32Pair, cos_out,
+                               sin_out, nullptr, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FLUX_OK : FLUX_ERR_CUDA;
+}
+
+int flux_rope_tables_packed(const int32_t *ids, int64_t S, const int32_t *axes_dims, int n_axes,
+                            double theta, uint32_t *table_out, void *stream) {
+  if (ids == nullptr || table_out == nullptr || axes_dims == nullptr) return FLUX_ERR_NULL;
+  if (S < 1 || S > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+  const cudaError_t e =
+      flux::launch_rope_tables(ids, S, nullptr, 0, pp, flux::TableFormat::kPackedF16, nullptr,
+                               nullptr, table_out, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? FLUX_OK : FLUX_ERR_CUDA;
 }
 
 size_t flux_joint_rope_attention_workspace(int64_t S, int D) {
   if (S < 1 || S > 0x7FFFFFFFLL || D <= 0 || (D & 1)) return 0;
-  return flux::kStatusBytes + 2 * flux::table_bytes(S, D);
+  return flux::kStatusBytes + flux::packed_table_bytes(S, D);
 }
 
 int flux_joint_rope_attention(const void *q, const void *k, const void *v,
@@ -103,30 +119,27 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
 
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  float *cos_t = reinterpret_cast<float *>(ws + flux::kStatusBytes);
-  float *sin_t = reinterpret_cast<float *>(ws + flux::kStatusBytes + flux::table_bytes(S, D));
+  uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
-  if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, cos_t, sin_t, st) !=
-      cudaSuccess)
+  if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
+                               nullptr, nullptr, table, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
-  if (flux::launch_joint_attention(q, k, v, out, cos_t, sin_t, status, B, S, H, st) !=
-      cudaSuccess)
+  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }
 
 int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
-                                     const float *cos_t, const float *sin_t, int B, int64_t S,
-                                     int H, int D, void *out, int32_t *status, void *stream) {
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || cos_t == nullptr ||
-      sin_t == nullptr || status == nullptr)
+                                     const uint32_t *table, int B, int64_t S, int H, int D,
+                                     void *out, int32_t *status, void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || table == nullptr ||
+      status == nullptr)
     return FLUX_ERR_NULL;
   if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
     return FLUX_ERR_SHAPE;
   if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(cos_t) ||
-      !aligned16(sin_t))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table))
     return FLUX_ERR_ALIGN;
   const size_t tensor_bytes = static_cast<size_t>(B) * static_cast<size_t>(S) *
                               static_cast<size_t>(H) * static_cast<size_t>(D) * 2;
@@ -135,7 +148,7 @@ int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v
     return FLUX_ERR_ALIAS;
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
-  if (flux::launch_joint_attention(q, k, v, out, cos_t, sin_t, status, B, S, H,
+  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H,
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;

@@ -1,6 +1,6 @@
-// Joint RoPE attention forward for sm_103a (GB300): tcgen05 MMAs with TMEM
-// accumulators, RoPE applied to Q and K while their tiles are staged into
-// shared memory.
+// Joint RoPE attention forward for sm_103a (GB300): warp-specialised, with
+// tcgen05 MMAs accumulating in tensor memory (TMEM), RoPE applied to Q and K
+// while their tiles are staged into shared memory, V staged by TMA.
 //
 // Definition ("Transformer架构解析FLUX.2-klein-base-9b-nvfp4", section 2:
 // scaled dot-product attention; "Diffusers 中 Flux2Transformer2DModel 全面解析",
@@ -8,18 +8,39 @@
 //   out[b, i, h, :] = sum_j softmax_j(q^_i . k^_j / sqrt(128)) v[b, j, h, :]
 // with q^, k^ the RoPE-rotated rows; non-causal over all S tokens.
 //
-// One CTA owns 128 query rows of one (batch, head). Per 128-key tile:
-//   1. all threads load K (rotating each adjacent channel pair with the
-//      token's cos/sin) and V into 128-byte-swizzled shared memory;
-//   2. one thread issues S = Q^ K^T as eight 128x128x16 tcgen05 MMAs into TMEM;
-//   3. each thread owns one query row (TMEM lane): it reads its 128 scores,
-//      runs the online softmax in the log2 domain, writes P as packed bf16
-//      and rescales its row of the running output O in TMEM;
-//   4. one thread issues O += P V (eight MMAs, V as an MN-major operand).
-// The epilogue divides O by the softmax denominator and stores bf16.
+// One CTA owns 256 query rows (two 128-row tiles Q0, Q1) of one (batch, head)
+// and walks every 128-key tile. 16 warps in four warpgroups:
+//   WG0  warp 0: TMA producer of raw Q (once), raw K tiles (2-stage ring) and
+//        the packed (cos, sin) table in 64-token halves (2-buffer ring);
+//        warp 1: MMA issuer (one thread); warp 2: TMEM allocation;
+//        warp 3: TMA producer of V tiles (2-stage ring).
+//   WG1  softmax of Q0: thread = TMEM lane = query row.
+//   WG2  softmax of Q1.
+//   WG3  RoPE: rotates each landed Q / K tile in place in shared memory,
+//        one adjacent channel pair per 32-bit word, with the table half
+//        that landed beside it, then hands the tile to the MMA.
+// Every global-to-shared copy is a TMA tile copy (128-byte swizzle for Q, K,
+// V; out-of-range tokens read as zeros); nothing on the path waits on a
+// plain global load.
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); the
+// softmax writes P_t as packed bf16 over the first 64 columns of S_t and the
+// MMA reads it from there (A operand in TMEM).
+//
+// Issue order of the MMA thread per key tile j:
+//   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
+// tcgen05 MMAs of one thread execute in order, so S_t(j+1) overwrites P_t(j)
+// only after PV_t(j) has read it, and the commit that signals S_t(j+1) also
+// covers PV_t(j): a softmax thread that sees S_t(j+1) may rescale O_t.
+//
+// Softmax runs in the log2 domain with a lazily updated running max: O and l
+// are rescaled only when a row's max grows by more than 8 (a factor 256),
+// which keeps exp2 arguments <= 8 and is exact after the final 1/l.
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 
 #include <cmath>
+#include <mutex>
 
 #include "flux_internal.h"
 #include "ptx_sm103a.cuh"
@@ -28,277 +49,485 @@ namespace flux {
 namespace {
 
 constexpr int kD = 128;
-constexpr int kBM = 128;
-constexpr int kBN = 128;
-constexpr int kThreads = 128;
-constexpr uint32_t kTileBytes = 128 * 128 * 2;  // 128 rows x 128 bf16
-constexpr uint32_t kBlockBytes = 16384;         // one 64-column swizzle block
+constexpr int kBM = 128;  // rows per Q tile
+constexpr int kBN = 128;  // keys per K/V tile
+constexpr int kQTiles = 2;
+constexpr int kRowsPerCta = kBM * kQTiles;
+constexpr int kThreads = 512;
+constexpr int kStages = 2;  // K and V ring depth
+constexpr int kPairs = kD / 2;
+constexpr uint32_t kTileBytes = 128 * 128 * 2;
+constexpr uint32_t kBlockBytes = 16384;          // one 64-channel swizzle block
+constexpr uint32_t kHalfRows = 64;               // table rows per table buffer
+constexpr uint32_t kTableHalfBytes = kHalfRows * kPairs * 4;  // 16 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
-#ifdef FLUX_P_VIA_SMEM
-constexpr bool kPInTmem = false;
-#else
-constexpr bool kPInTmem = true;
-#endif
+// Shared-memory map (offsets from a 1024-byte aligned base).
+constexpr uint32_t kOffQ = 0;                                   // Q0, Q1
+constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;         // K ring
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;         // V ring
+constexpr uint32_t kOffT = kOffV + kStages * kTileBytes;         // table halves (2)
+constexpr uint32_t kOffBar = kOffT + 2 * kTableHalfBytes;        // mbarriers
+// barrier indices
+constexpr int kBarQRaw = 0;
+constexpr int kBarQFull = 1;
+constexpr int kBarKRaw = 2;                  // + stage
+constexpr int kBarKFull = kBarKRaw + kStages;
+constexpr int kBarKEmpty = kBarKFull + kStages;
+constexpr int kBarVFull = kBarKEmpty + kStages;
+constexpr int kBarVEmpty = kBarVFull + kStages;
+constexpr int kBarTFull = kBarVEmpty + kStages;  // + table buffer
+constexpr int kBarTEmpty = kBarTFull + 2;
+constexpr int kBarSFull = kBarTEmpty + 2;  // + q tile
+constexpr int kBarPFull = kBarSFull + kQTiles;
+constexpr int kBarODone = kBarPFull + kQTiles;
+constexpr int kBarDrain = kBarODone + kQTiles;
+constexpr int kNumBars = kBarDrain + 1;
+constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
-constexpr uint32_t kNumTiles = kPInTmem ? 3 : 4;  // Q, K, V (+ P)
-constexpr uint32_t kCtrlOffset = kNumTiles * kTileBytes;
-constexpr uint32_t kSmemBytes = kCtrlOffset + 64 + 1024;  // + control block + alignment slack
-constexpr uint32_t kTmemCols = 256;                        // S: 0..127, O: 128..255
+// Register split (setmaxnreg): 512 threads x 128 registers at launch.
+constexpr uint32_t kRegsSoftmax = 168;
+constexpr uint32_t kRegsOther = 88;
+static_assert(128 * (2 * kRegsSoftmax + 2 * kRegsOther) == 512 * 128,
+              "warpgroup register shares must add up to the launch allocation");
 
-// Byte offset of 16-byte chunk c16 (0..15) of row r in a [128 x 128] bf16
-// tile stored as two 64-column blocks, each rows of 128 bytes with the
-// 128-byte swizzle (chunk index XOR row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c16) {
   return static_cast<uint32_t>((c16 >> 3) * kBlockBytes + r * 128 + (((c16 & 7) ^ (r & 7)) << 4));
 }
 
-// K-major operand (rows = M or N, 128 channels = K): slice kk covers
-// channels [16 kk, 16 kk + 16).
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int kk) {
   return sdesc_sw128(tile + (kk >> 2) * kBlockBytes + (kk & 3) * 32, 16, 1024);
 }
 
-// V as the MN-major B operand of P V: rows = keys (K), columns = channels
-// (N). Slice kk covers keys [16 kk, 16 kk + 16); the two 64-channel blocks
-// are kBlockBytes apart.
 __device__ __forceinline__ uint64_t desc_v(uint32_t tile, int kk) {
   return sdesc_sw128(tile + kk * 2048, kBlockBytes, 1024);
 }
 
-// Rotate the two bf16 channels packed in `w` by (c, s) and round back.
-__device__ __forceinline__ uint32_t rope_pair(uint32_t w, float c, float s) {
+// Rotate the two bf16 channels packed in `w` by the fp16 (cos, sin) in `cs`.
+__device__ __forceinline__ uint32_t rope_pair(uint32_t w, uint32_t cs) {
   const float x0 = bf16lo_to_f32(w), x1 = bf16hi_to_f32(w);
+  const float c = f16lo_to_f32(cs), s = f16hi_to_f32(cs);
   return pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
 }
 
-// Stage a [128 tokens x 128 channels] tile of one head into swizzled smem,
-// rotating it with the tokens' table rows when kRotate. Rows at or past
-// `rows_valid` are written as zeros.
-template <bool kRotate>
-__device__ __forceinline__ void stage_tile(uint32_t sdst, const uint16_t *g, int64_t row_stride,
-                                           int rows_valid, const float *cos_t,
-                                           const float *sin_t) {
-#pragma unroll 4
-  for (int i = 0; i < (kBM * 16) / kThreads; ++i) {
-    const int x = i * kThreads + static_cast<int>(threadIdx.x);
-    const int r = x >> 4, c16 = x & 15;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r < rows_valid) {
-      w = ld_global_nc_v4(g + r * row_stride + c16 * 8);
-      if (kRotate) {
-        const float4 c = ld_global_nc_f4(cos_t + r * (kD / 2) + c16 * 4);
-        const float4 s = ld_global_nc_f4(sin_t + r * (kD / 2) + c16 * 4);
-        w.x = rope_pair(w.x, c.x, s.x);
-        w.y = rope_pair(w.y, c.y, s.y);
-        w.z = rope_pair(w.z, c.z, s.z);
-        w.w = rope_pair(w.w, c.w, s.w);
-      }
-    }
-    st_shared_v4(sdst + sw128_offset(r, c16), w);
+template <uint32_t kRegs>
+__device__ __forceinline__ void reg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void reg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+
+// 128 RoPE threads rotate rows [64 half, 64 half + 64) of a swizzled tile in
+// place with the table half at `tbl` ([64 rows][64 pairs] uint32). Thread u
+// owns 16-byte column chunk u & 15 (channel pairs 4(u&15) .. +3) of every
+// 8th row.
+__device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u) {
+  const int c16 = u & 15;
+  const int rsub = u >> 4;
+  uint4 w[8], cs[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rh = i * 8 + rsub;
+    w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
+    cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int rh = i * 8 + rsub;
+    uint4 o;
+    o.x = rope_pair(w[i].x, cs[i].x);
+    o.y = rope_pair(w[i].y, cs[i].y);
+    o.z = rope_pair(w[i].z, cs[i].z);
+    o.w = rope_pair(w[i].w, cs[i].w);
+    st_shared_v4(tile + sw128_offset(half * 64 + rh, c16), o);
   }
 }
 
+struct Maps {
+  CUtensorMap q, k, v, table;
+};
+
 __global__ void __launch_bounds__(kThreads, 1)
-    joint_rope_attention_kernel(const uint16_t *__restrict__ q, const uint16_t *__restrict__ k,
-                                const uint16_t *__restrict__ v, uint16_t *__restrict__ out,
-                                const float *__restrict__ cos_t, const float *__restrict__ sin_t,
+    joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
                                 int *__restrict__ status, int64_t S, int H) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
-  const uint32_t sQ = smem_addr(base);
-  const uint32_t sK = sQ + kTileBytes;
-  const uint32_t sV = sK + kTileBytes;
-  const uint32_t sP = sV + kTileBytes;  // used only when P goes through smem
-  uint64_t *bar_mma = reinterpret_cast<uint64_t *>(base + kCtrlOffset);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kCtrlOffset + 8);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kCtrlOffset + 12);
+  const uint32_t sbase = smem_addr(base);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(base + kOffTmemSlot);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(base + kOffAbort);
 
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5;
-  const int m0 = static_cast<int>(blockIdx.x) * kBM;
+  const int lane = tid & 31;
+  const int m0 = static_cast<int>(blockIdx.x) * kRowsPerCta;
   const int h = static_cast<int>(blockIdx.y);
   const int b = static_cast<int>(blockIdx.z);
   const int64_t row_stride = static_cast<int64_t>(H) * kD;
-  const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;  // token 0 of (b, h)
-  const uint16_t *qh = q + head0;
-  const uint16_t *kh = k + head0;
-  const uint16_t *vh = v + head0;
+  const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;
+  const int n_tiles = static_cast<int>((S + kBN - 1) / kBN);
 
   if (tid == 0) {
-    mbar_init(smem_addr(bar_mma), 1);
+    mbar_init(bar(kBarQRaw), 1);
+    mbar_init(bar(kBarQFull), 128);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kBarKRaw + s), 1);
+      mbar_init(bar(kBarKFull + s), 128);
+      mbar_init(bar(kBarKEmpty + s), 1);
+      mbar_init(bar(kBarVFull + s), 1);
+      mbar_init(bar(kBarVEmpty + s), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(kBarTFull + i), 1);
+      mbar_init(bar(kBarTEmpty + i), 128);
+    }
+    for (int t = 0; t < kQTiles; ++t) {
+      mbar_init(bar(kBarSFull + t), 1);
+      mbar_init(bar(kBarPFull + t), 128);
+      mbar_init(bar(kBarODone + t), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 2) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
-
-  const int q_valid = static_cast<int>(S - m0 < kBM ? S - m0 : kBM);
-  stage_tile<true>(sQ, qh + m0 * row_stride, row_stride, q_valid, cos_t + m0 * (kD / 2),
-                   sin_t + m0 * (kD / 2));
-  fence_proxy_async_smem();
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;        // scores, later P (packed bf16 in columns 0..63)
-  const uint32_t tO = tmem + 128;  // running output
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+
   const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
   const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
-  const uint32_t bar = smem_addr(bar_mma);
-  // softmax in the log2 domain: x = s * log2(e) / sqrt(128)
-  const float scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
 
-  float m_run = -INFINITY, l_run = 0.f;
-  uint32_t phase = 0;
-  const int n_tiles = static_cast<int>((S + kBN - 1) / kBN);
-
-  for (int jt = 0; jt < n_tiles; ++jt) {
-    const int n0 = jt * kBN;
-    const int kv_valid = static_cast<int>(S - n0 < kBN ? S - n0 : kBN);
-    // The previous P V has completed (waited below), so K/V/P are free.
-    stage_tile<true>(sK, kh + n0 * row_stride, row_stride, kv_valid, cos_t + n0 * (kD / 2),
-                     sin_t + n0 * (kD / 2));
-    stage_tile<false>(sV, vh + n0 * row_stride, row_stride, kv_valid, nullptr, nullptr);
-    fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
+  if (warp < 4) {
+    reg_dec<kRegsOther>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------- producer: Q, K (raw) and table
+      tma_prefetch_desc(&maps.q);
+      tma_prefetch_desc(&maps.k);
+      tma_prefetch_desc(&maps.table);
+      mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
+      for (int t = 0; t < kQTiles; ++t) {
+        const uint32_t dst = sbase + kOffQ + t * kTileBytes;
+        tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
+        tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
+      }
+      int g = 0;  // table halves issued so far
+      bool ok = true;
+      auto table_half = [&](int row0) {
+        const int buf = g & 1;
+        const uint32_t use = static_cast<uint32_t>(g >> 1);
+        if (!(ok = mbar_wait(bar(kBarTEmpty + buf), (use & 1u) ^ 1u, abort_flag))) return;
+        mbar_arrive_expect_tx(bar(kBarTFull + buf), kTableHalfBytes);
+        tma_load_2d(sbase + kOffT + buf * kTableHalfBytes, &maps.table, bar(kBarTFull + buf), 0,
+                    row0);
+        ++g;
+      };
+      for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % kStages;
+        const uint32_t use = static_cast<uint32_t>(j / kStages);
+        if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
+        const uint32_t dst = sbase + kOffK + s * kTileBytes;
+        mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
+        tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, j * kBN, b);
+        tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, j * kBN, b);
+        table_half(j * kBN);
+        if (ok) table_half(j * kBN + static_cast<int>(kHalfRows));
+      }
+    } else if (warp == 3 && lane == 0) {
+      // ------------------------------------------------------ producer: V
+      tma_prefetch_desc(&maps.v);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages;
+        const uint32_t use = static_cast<uint32_t>(j / kStages);
+        if (!mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag)) break;
+        const uint32_t dst = sbase + kOffV + s * kTileBytes;
+        mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
+        tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, j * kBN, b);
+        tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, j * kBN, b);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // ------------------------------------------------------ MMA issuer
+      // TMEM: S_t at column 128 t, O_t at 256 + 128 t; Q_t at kOffQ + t * kTileBytes
+      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
+      ok = ok && mbar_wait(bar(kBarKFull + 0), 0, abort_flag);
+      if (ok) {
+        tc_fence_after_sync();
+        const uint32_t sK = sbase + kOffK;
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk)
+            mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
+                   desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
+          mma_commit(bar(kBarSFull + t));
+        }
+        mma_commit(bar(kBarKEmpty + 0));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int sv = j % kStages;
+        const uint32_t sV = sbase + kOffV + sv * kTileBytes;
+        const bool more = j + 1 < n_tiles;
+        const int sk = (j + 1) % kStages;
+        const uint32_t sK = sbase + kOffK + sk * kTileBytes;
+        if (!(ok = mbar_wait(bar(kBarVFull + sv), static_cast<uint32_t>(j / kStages) & 1u,
+                             abort_flag)))
+          break;
+#pragma unroll
+        for (int t = 0; t < kQTiles; ++t) {
+          if (!(ok = mbar_wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, abort_flag))) break;
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_v(sV, kk), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(bar(kBarODone + t));
+          if (t == kQTiles - 1) mma_commit(bar(kBarVEmpty + sv));
+          if (more) {
+            if (t == 0 &&
+                !(ok = mbar_wait(bar(kBarKFull + sk), static_cast<uint32_t>((j + 1) / kStages) & 1u,
+                                 abort_flag)))
+              break;
+            tc_fence_after_sync();
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+              mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
+                     desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
+            mma_commit(bar(kBarSFull + t));
+            if (t == kQTiles - 1) mma_commit(bar(kBarKEmpty + sk));
+          }
+        }
+      }
+      // drain: every MMA issued above has finished before TMEM is released
+      mma_commit(bar(kBarDrain));
+      const long long t0 = clock64();
+      while (!mbar_try_wait(bar(kBarDrain), 0) && clock64() - t0 < kWaitBudgetCycles) {
+      }
+    }
+  } else if (warp < 12) {
+    // ---------------------------------------------------------- softmax
+    reg_inc<kRegsSoftmax>();
+    const int t = (warp - 4) >> 2;  // Q tile
+    const int wq = warp & 3;        // TMEM lane quadrant
+    const int row = wq * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + t * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + t * 128 + lane_off;
+    const float scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!(ok = mbar_wait(bar(kBarSFull + t), static_cast<uint32_t>(j) & 1u, abort_flag))) break;
       tc_fence_after_sync();
+      uint32_t sr[kBN];
 #pragma unroll
-      for (int kk = 0; kk < kD / 16; ++kk)
-        mma_ss(tS, desc_kmajor(sQ, kk), desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
-      mma_commit(bar);
+      for (int c = 0; c < kBN / 32; ++c)
+        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tmem_ld_wait();
+      const int valid = static_cast<int>(S - static_cast<int64_t>(j) * kBN);
+      float mx = -INFINITY;
+      if (valid >= kBN) {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
+          mx = fmaxf(mx, __uint_as_float(sr[i]));
+        }
+      }
+      mx *= scale_log2;
+      float alpha = 1.f;
+      float m_use = m_run;
+      if (j == 0) {
+        m_use = mx;
+      } else if (__any_sync(0xffffffffu, mx > m_run + kRescaleThreshold)) {
+        m_use = fmaxf(m_run, mx);
+        alpha = ex2_approx(m_run - m_use);
+        // S_t(j) is complete, hence so is PV_t(j-1): O_t is stable here.
+#pragma unroll 1
+        for (int c = 0; c < kD / 16; ++c) {
+          uint32_t o[16];
+          tmem_ld16(tO + c * 16, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st16(tO + c * 16, o);
+        }
+      }
+      const float neg_m = -m_use;
+      float sum = 0.f;
+      // P in four chunks of 32 keys (16 packed columns each) to bound registers
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c * 32 + i]), scale_log2, neg_m));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c * 32 + i + 1]), scale_log2, neg_m));
+          sum += p0 + p1;
+          pk[i / 2] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, pk);
+      }
+      tmem_st_wait();
+      l_run = l_run * alpha + sum;
+      m_run = m_use;
+      tc_fence_before_sync();
+      mbar_arrive(bar(kBarPFull + t));
     }
-    mbar_wait(bar, phase, abort_flag);
-    phase ^= 1u;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-
-    // ---- online softmax on this thread's row
-    uint32_t sr[kBN];
-#pragma unroll
-    for (int c = 0; c < kBN / 32; ++c)
-      tmem_ld32(tS + lane_off + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-    tmem_ld_wait();
-    float mx = m_run;
-#pragma unroll
-    for (int j = 0; j < kBN; ++j) {
-      const float x = (j < kv_valid) ? __uint_as_float(sr[j]) * scale_log2 : -INFINITY;
-      sr[j] = __float_as_uint(x);
-      mx = fmaxf(mx, x);
-    }
-    const float alpha = ex2_approx(m_run - mx);  // 0 on the first tile
-    float sum = 0.f;
-    uint32_t pk[kBN / 2];
-#pragma unroll
-    for (int j = 0; j < kBN; j += 2) {
-      const float p0 = ex2_approx(__uint_as_float(sr[j]) - mx);
-      const float p1 = ex2_approx(__uint_as_float(sr[j + 1]) - mx);
-      sum += p0 + p1;
-      pk[j / 2] = pack_bf16x2(p0, p1);
-    }
-    l_run = l_run * alpha + sum;
-    m_run = mx;
-
-    if (kPInTmem) {
-      tmem_st32(tS + lane_off, *reinterpret_cast<uint32_t(*)[32]>(&pk[0]));
-      tmem_st32(tS + lane_off + 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[32]));
-    } else {
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16)
-        st_shared_v4(sP + sw128_offset(tid, c16),
-                     make_uint4(pk[4 * c16], pk[4 * c16 + 1], pk[4 * c16 + 2], pk[4 * c16 + 3]));
-    }
-    if (jt > 0) {
+    if (ok && mbar_wait(bar(kBarODone + t), static_cast<uint32_t>(n_tiles - 1) & 1u, abort_flag)) {
+      tc_fence_after_sync();
+      const float inv_l = 1.f / l_run;
+      const int64_t token = static_cast<int64_t>(m0) + t * kBM + row;
+      uint16_t *orow = out + head0 + token * row_stride;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tO + lane_off + c * 32, o);
+        tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
+        if (token < S) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-        tmem_st32(tO + lane_off + c * 32, o);
-      }
-    }
-    tmem_st_wait();
-    if (!kPInTmem) fence_proxy_async_smem();
-    tc_fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after_sync();
-#pragma unroll
-      for (int kk = 0; kk < kBN / 16; ++kk) {
-        const uint32_t acc = (jt > 0 || kk > 0) ? 1u : 0u;
-        if (kPInTmem)
-          mma_ts(tO, tS + kk * 8, desc_v(sV, kk), idesc_pv, acc);
-        else
-          mma_ss(tO, desc_kmajor(sP, kk), desc_v(sV, kk), idesc_pv, acc);
-      }
-      mma_commit(bar);
-    }
-    mbar_wait(bar, phase, abort_flag);
-    phase ^= 1u;
-    __syncthreads();
-    if (*abort_flag) break;
-    tc_fence_after_sync();
-  }
-
-  if (!*abort_flag) {
-    const float inv_l = 1.f / l_run;
-    const int r = tid;
-    uint16_t *orow = out + head0 + static_cast<int64_t>(m0 + r) * row_stride;
-#pragma unroll
-    for (int c = 0; c < kD / 32; ++c) {
-      uint32_t o[32];
-      tmem_ld32(tO + lane_off + c * 32, o);
-      tmem_ld_wait();
-      if (r < q_valid) {
-#pragma unroll
-        for (int j = 0; j < 32; j += 8) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(o[j]) * inv_l, __uint_as_float(o[j + 1]) * inv_l);
-          w.y = pack_bf16x2(__uint_as_float(o[j + 2]) * inv_l, __uint_as_float(o[j + 3]) * inv_l);
-          w.z = pack_bf16x2(__uint_as_float(o[j + 4]) * inv_l, __uint_as_float(o[j + 5]) * inv_l);
-          w.w = pack_bf16x2(__uint_as_float(o[j + 6]) * inv_l, __uint_as_float(o[j + 7]) * inv_l);
-          *reinterpret_cast<uint4 *>(orow + c * 32 + j) = w;
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
+            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = w;
+          }
         }
       }
     }
-  } else if (tid == 0) {
-    atomicExch(status, FLUX_ERR_DEVICE_TIMEOUT);
+  } else {
+    // --------------------------------------------------------- RoPE warps
+    reg_dec<kRegsOther>();
+    const int u = tid - 384;
+    int g = 0;  // table halves consumed so far
+    bool ok = mbar_wait(bar(kBarQRaw), 0, abort_flag);
+    auto rotate_tile = [&](uint32_t tile) {
+      for (int half = 0; ok && half < 2; ++half) {
+        const int buf = g & 1;
+        if (!(ok = mbar_wait(bar(kBarTFull + buf), static_cast<uint32_t>(g >> 1) & 1u, abort_flag)))
+          return;
+        rotate_half(tile, sbase + kOffT + buf * kTableHalfBytes, half, u);
+        mbar_arrive(bar(kBarTEmpty + buf));
+        ++g;
+      }
+    };
+    for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes);
+    if (ok) {
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kBarQFull));
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
+      const int s = j % kStages;
+      if (!(ok = mbar_wait(bar(kBarKRaw + s), static_cast<uint32_t>(j / kStages) & 1u, abort_flag)))
+        break;
+      rotate_tile(sbase + kOffK + s * kTileBytes);
+      if (!ok) break;
+      fence_proxy_async_smem();
+      mbar_arrive(bar(kBarKFull + s));
+    }
   }
+
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 2) {
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
+  if (tid == 0 && *abort_flag) atomicExch(status, FLUX_ERR_DEVICE_TIMEOUT);
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// q, k or v as a 4-D tensor (D, H, S, B); one box = 64 channels x 128 tokens
+// of one head, 128-byte swizzled; out-of-range tokens read as zeros.
+bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
+                                 static_cast<cuuint64_t>(H) * kD * 2,
+                                 static_cast<cuuint64_t>(S) * H * kD * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The packed table [S, 64] uint32 as a 2-D tensor; one box = 64 tokens.
+bool make_table_map(CUtensorMap *map, const uint32_t *table, int64_t S) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPairs), static_cast<cuuint64_t>(S)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kPairs) * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kPairs), kHalfRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(table), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
-                                   const float *cos_t, const float *sin_t, int *status, int B,
-                                   int64_t S, int H, cudaStream_t stream) {
-  static bool attr_done = false;  // per process; the attribute is per function
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(joint_rope_attention_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
-  const dim3 grid(static_cast<unsigned>((S + kBM - 1) / kBM), static_cast<unsigned>(H),
-                  static_cast<unsigned>(B));
+                                   const uint32_t *table, int *status, int B, int64_t S, int H,
+                                   cudaStream_t stream) {
+  static std::once_flag attr_once[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaError_t attr_err = cudaSuccess;
+  std::call_once(attr_once[dev], [&] {
+    attr_err = cudaFuncSetAttribute(joint_rope_attention_kernel,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    static_cast<int>(kSmemBytes));
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  Maps maps;
+  if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
+      !make_head_map(&maps.v, v, B, S, H) || !make_table_map(&maps.table, table, S))
+    return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>((S + kRowsPerCta - 1) / kRowsPerCta),
+                  static_cast<unsigned>(H), static_cast<unsigned>(B));
   joint_rope_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k),
-      static_cast<const uint16_t *>(v), static_cast<uint16_t *>(out), cos_t, sin_t, status, S, H);
+      maps, static_cast<uint16_t *>(out), status, S, H);
   return cudaGetLastError();
 }
 

@@ -27,23 +27,30 @@ struct RopePairs {
 // Fills `pp` from host axes_dims; returns FLUX_OK or FLUX_ERR_AXES.
 int make_rope_pairs(const int32_t *axes_dims, int n_axes, double theta, RopePairs *pp);
 
-// Enqueues the table kernel over the joint id sequence [seg0 ; seg1].
+// Output formats of the table kernel.
+enum class TableFormat {
+  kF32Pair,    // cos [S, P] and sin [S, P] fp32 (flux_rope_tables)
+  kPackedF16,  // one uint32 per (token, pair): fp16 cos in bits 0-15, fp16 sin in 16-31
+};
+
+// Enqueues the table kernel over the joint id sequence [seg0 ; seg1]. For
+// kPackedF16 the table goes to `packed` ([S, P] uint32) and cos/sin are unused.
 cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *ids1, int64_t S1,
-                               const RopePairs &pp, float *cos_out, float *sin_out,
-                               cudaStream_t stream);
+                               const RopePairs &pp, TableFormat fmt, float *cos_out,
+                               float *sin_out, uint32_t *packed, cudaStream_t stream);
 
 // Workspace layout of flux_joint_rope_attention: a 256-byte status block,
-// then cos [S, D/2] and sin [S, D/2] fp32, each padded to 256 bytes.
+// then the packed table [S, D/2] uint32, padded to 256 bytes.
 constexpr size_t kStatusBytes = 256;
-inline size_t table_bytes(int64_t S, int D) {
-  size_t b = static_cast<size_t>(S) * static_cast<size_t>(D / 2) * sizeof(float);
+inline size_t packed_table_bytes(int64_t S, int D) {
+  size_t b = static_cast<size_t>(S) * static_cast<size_t>(D / 2) * sizeof(uint32_t);
   return (b + 255) & ~static_cast<size_t>(255);
 }
 
-// Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; cos/sin
-// are the tables of the joint sequence; status is the device status word.
+// Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`
+// is the packed table of the joint sequence; status is the device status word.
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
-                                   const float *cos_t, const float *sin_t, int *status, int B,
-                                   int64_t S, int H, cudaStream_t stream);
+                                   const uint32_t *table, int *status, int B, int64_t S, int H,
+                                   cudaStream_t stream);
 
 }  // namespace flux

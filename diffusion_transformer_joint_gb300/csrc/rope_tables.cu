@@ -11,6 +11,14 @@
 // Cody-Waite step (Cody & Waite, "Software Manual for the Elementary
 // Functions", 1980) to r in [-pi, pi]; cosine and sine are then taken in
 // fp32 on r. This keeps the kernel off the slow fp64 transcendental path.
+//
+// Two output formats: separate fp32 cos and sin arrays (the public table
+// call), or one 32-bit word per (token, pair) holding fp16 cos and sin, the
+// format the attention kernel stages by TMA next to each K tile (half the
+// bytes; fp16 keeps |error| <= 2^-12, below the bf16 rounding of the rotated
+// channels it multiplies).
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 #include "flux_internal.h"
@@ -23,12 +31,14 @@ constexpr double kTwoPiHi = 6.283185307179586;
 constexpr double kTwoPiLo = 2.4492935982947064e-16;
 constexpr double kInvTwoPi = 0.15915494309189535;
 
+template <TableFormat kFmt>
 __global__ void __launch_bounds__(256) rope_tables_kernel(const int32_t *__restrict__ ids0,
                                                           int64_t S0,
                                                           const int32_t *__restrict__ ids1,
                                                           int64_t S, const RopePairs pp,
                                                           float *__restrict__ cos_out,
-                                                          float *__restrict__ sin_out) {
+                                                          float *__restrict__ sin_out,
+                                                          uint32_t *__restrict__ packed) {
   __shared__ double omega[kMaxPairs];
   const int P = pp.n_pairs;
   for (int p = threadIdx.x; p < P; p += blockDim.x)
@@ -47,8 +57,13 @@ __global__ void __launch_bounds__(256) rope_tables_kernel(const int32_t *__restr
     r = fma(-kq, kTwoPiLo, r);
     float sn, cs;
     sincosf(static_cast<float>(r), &sn, &cs);
-    cos_out[e] = cs;
-    sin_out[e] = sn;
+    if constexpr (kFmt == TableFormat::kF32Pair) {
+      cos_out[e] = cs;
+      sin_out[e] = sn;
+    } else {
+      packed[e] = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(cs))) |
+                  (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(sn))) << 16);
+    }
   }
 }
 
@@ -75,15 +90,19 @@ int make_rope_pairs(const int32_t *axes_dims, int n_axes, double theta, RopePair
 }
 
 cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *ids1, int64_t S1,
-                               const RopePairs &pp, float *cos_out, float *sin_out,
-                               cudaStream_t stream) {
+                               const RopePairs &pp, TableFormat fmt, float *cos_out,
+                               float *sin_out, uint32_t *packed, cudaStream_t stream) {
   const int64_t S = S0 + S1;
   const int64_t total = S * pp.n_pairs;
   int64_t blocks = (total + 255) / 256;
   if (blocks > 4 * 152) blocks = 4 * 152;
   if (blocks < 1) blocks = 1;
-  rope_tables_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(ids0, S0, ids1, S, pp,
-                                                                        cos_out, sin_out);
+  if (fmt == TableFormat::kF32Pair)
+    rope_tables_kernel<TableFormat::kF32Pair><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        ids0, S0, ids1, S, pp, cos_out, sin_out, packed);
+  else
+    rope_tables_kernel<TableFormat::kPackedF16><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        ids0, S0, ids1, S, pp, cos_out, sin_out, packed);
   return cudaGetLastError();
 }
 

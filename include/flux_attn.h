@@ -86,10 +86,23 @@ int flux_rope_tables(const int32_t *ids, int64_t S, const int32_t *axes_dims, in
                      double theta, float *cos_out, float *sin_out, void *stream);
 
 /*
+ * flux_rope_tables_packed: the same table, one 32-bit word per (token, pair):
+ * fp16 cos in bits 0-15 and fp16 sin in bits 16-31 (round to nearest even,
+ * |error| <= 2^-12). This is the format the attention kernel stages next to
+ * each key tile; flux_joint_rope_attention_tabled takes it.
+ *
+ *   ids, S, axes_dims, n_axes, theta, stream  as for flux_rope_tables.
+ *   table_out  device, uint32 [S, sum(axes_dims)/2] row-major, 16-byte aligned.
+ */
+int flux_rope_tables_packed(const int32_t *ids, int64_t S, const int32_t *axes_dims, int n_axes,
+                            double theta, uint32_t *table_out, void *stream);
+
+/*
  * flux_joint_rope_attention_workspace: bytes of device workspace that
  * flux_joint_rope_attention needs for a joint sequence of S tokens and head
- * width D (the RoPE tables, 2 * S * (D/2) fp32, plus a 256-byte status
- * block). Returns 0 when S < 1 or D is not positive and even.
+ * width D: a 256-byte status block plus the packed RoPE table
+ * (S * (D/2) * 4 bytes, rounded up to 256). Returns 0 when S < 1 or D is not
+ * positive and even.
  */
 size_t flux_joint_rope_attention_workspace(int64_t S, int D);
 
@@ -114,9 +127,10 @@ size_t flux_joint_rope_attention_workspace(int64_t S, int D);
  *              call before the attention kernel runs.
  *   stream     cudaStream_t as void*.
  *
- * Numerics: bf16 inputs, RoPE applied in fp32 and rounded to bf16 for the
- * tensor-core products, fp32 accumulation and softmax, bf16 output rounded
- * to nearest even.
+ * Numerics: bf16 inputs; the RoPE table is built in fp64/fp32 and stored as
+ * fp16 (cos, sin) pairs; the rotation runs in fp32 and is rounded to bf16 for
+ * the tensor-core products; fp32 accumulation and softmax; P is rounded to
+ * bf16 for the P V product; bf16 output rounded to nearest even.
  *
  * Returns FLUX_OK when both kernels were enqueued, else a negative status.
  * Requires an sm_103 device (GB300).
@@ -128,14 +142,14 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
                               void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * flux_joint_rope_attention_tabled: the same attention, with the RoPE tables
- * supplied by the caller (built once by flux_rope_tables for the joint id
- * sequence and reused, e.g. by every attention layer of one denoiser step:
+ * flux_joint_rope_attention_tabled: the same attention, with the RoPE table
+ * supplied by the caller (built once by flux_rope_tables_packed for the joint
+ * id sequence and reused, e.g. by every attention layer of one denoiser step:
  * the position ids do not change between layers).
  *
  *   q, k, v, out  as for flux_joint_rope_attention, [B, S, H, D], D == 128.
- *   cos_t, sin_t  device, fp32 [S, D/2] as written by flux_rope_tables; 16-byte
- *                 aligned.
+ *   table         device, uint32 [S, D/2] as written by flux_rope_tables_packed;
+ *                 16-byte aligned.
  *   status        device int32 word; the kernel writes FLUX_ERR_DEVICE_TIMEOUT
  *                 there if a bounded wait runs out and never writes it
  *                 otherwise (the caller clears it).
@@ -143,8 +157,8 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
  * Returns FLUX_OK when the kernel was enqueued, else a negative status.
  */
 int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
-                                     const float *cos_t, const float *sin_t, int B, int64_t S,
-                                     int H, int D, void *out, int32_t *status, void *stream);
+                                     const uint32_t *table, int B, int64_t S, int H, int D,
+                                     void *out, int32_t *status, void *stream);
 
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)

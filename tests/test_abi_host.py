@@ -41,9 +41,9 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    assert lib.flux_joint_rope_attention_workspace(4608, 128) == 256 + 2 * 4608 * 64 * 4
-    assert lib.flux_joint_rope_attention_workspace(80, 128) == 256 + 2 * 20480
-    assert lib.flux_joint_rope_attention_workspace(1, 128) == 256 + 2 * 256
+    assert lib.flux_joint_rope_attention_workspace(4608, 128) == 256 + 4608 * 64 * 4
+    assert lib.flux_joint_rope_attention_workspace(80, 128) == 256 + 20480
+    assert lib.flux_joint_rope_attention_workspace(1, 128) == 256 + 256
     assert lib.flux_joint_rope_attention_workspace(0, 128) == 0
     assert lib.flux_joint_rope_attention_workspace(10, 7) == 0
 
@@ -96,3 +96,6 @@ def test_rope_tables_bad_arguments(lib):
     assert lib.flux_rope_tables(P(16), 0, axes, 4, 2000.0, P(16), P(32), None) == -2
     bad = (ctypes.c_int32 * 2)(3, 4)
     assert lib.flux_rope_tables(P(16), 4, bad, 2, 2000.0, P(16), P(32), None) == -3
+    assert lib.flux_rope_tables_packed(None, 4, axes, 4, 2000.0, P(16), None) == -1
+    assert lib.flux_rope_tables_packed(P(16), 0, axes, 4, 2000.0, P(16), None) == -2
+    assert lib.flux_rope_tables_packed(P(16), 4, bad, 2, 2000.0, P(16), None) == -3

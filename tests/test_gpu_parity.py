@@ -74,6 +74,31 @@ def test_rope_tables_match_oracle(lo, hi, tol):
     assert np.abs(s.cpu().numpy() - rs).max() <= tol
 
 
+def test_packed_rope_table_matches_oracle():
+    # fp16 (cos, sin): round-to-nearest on values in [-1, 1] is within 2^-12
+    ids = W.random_ids(999, seed=6, low=-70000, high=70000)
+    packed = binding.rope_tables_packed(_dev(ids))
+    torch.cuda.synchronize()
+    c, s = binding.unpack_table(packed)
+    rc, rs = oracle.rope_tables(ids)
+    assert np.abs(c.cpu().numpy() - rc).max() <= 2.0 ** -12 + 2e-6
+    assert np.abs(s.cpu().numpy() - rs).max() <= 2.0 ** -12 + 2e-6
+
+
+def test_tabled_entry_matches_one_call_entry():
+    w = W.WORKLOADS["tiny"]
+    q, k, v = (t.cuda() for t in W.workload_qkv(w))
+    txt, img = W.workload_ids(w)
+    ids = _dev(np.concatenate([txt, img]))
+    table = binding.rope_tables_packed(ids)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    a = binding.joint_rope_attention_tabled(q, k, v, table, status)
+    b = binding.joint_rope_attention(q, k, v, _dev(txt), _dev(img))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(a, b)
+
+
 def test_rope_tables_zero_ids_are_identity():
     c, s = binding.rope_tables(torch.zeros((300, 4), dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
@@ -126,15 +151,18 @@ def test_large_ids():
 def test_peaked_softmax_online_rescale():
     """q scaled by 8: logits of order 8, so the running max moves across key tiles.
 
-    At this logit scale the bf16 rounding of the rotated q and k alone moves a
-    logit by ~0.03 (8 * sqrt(2) * 2^-8 / sqrt(3)), which a bf16-operand kernel
-    cannot avoid; so the reference here is the oracle's own rotation, rounded
-    to bf16 by torch, fed to the oracle's attention with zero ids (identity
-    rotation). What remains is the softmax / rescale / P V path. There the
-    bf16 rounding of each softmax weight (unit roundoff u = 2^-9), with the
-    denominator summed from the unrounded fp32 weights, perturbs an output by
-    at most about 2 u max|v| when one weight dominates; the max-abs bound is
-    that plus the standard 1e-2, the mean-abs bound stays 1e-3.
+    At this logit scale, storage roundings that any bf16-operand kernel makes
+    move logits by several hundredths: the bf16 rounding of the rotated q and
+    k (~0.03 here) and, in this kernel, the fp16 storage of the (cos, sin)
+    table, which flips the bf16 rounding of a few percent of rotated channels.
+    So the reference applies the same storage formats to the oracle's own
+    values: the oracle's tables rounded to fp16, the oracle's rotation with
+    those tables rounded to bf16, then the oracle's attention with zero ids
+    (identity rotation). What remains is the softmax / rescale / P V path.
+    There the bf16 rounding of each softmax weight (unit roundoff u = 2^-9),
+    with the denominator summed from the unrounded fp32 weights, perturbs an
+    output by at most about 2 u max|v| when one weight dominates; the max-abs
+    bound is that plus the standard 1e-2, the mean-abs bound stays 1e-3.
     """
     B, H, S = 1, 2, 517
     q = W.normal_bf16((B, S, H, 128), 45, scale=8.0)
@@ -143,8 +171,10 @@ def test_peaked_softmax_online_rescale():
     ids = W.random_ids(S, 48, 0, 600)
     out = _run_gpu(q, k, v, ids[:33], ids[33:])
     c, s = oracle.rope_tables(ids)
-    qr = torch.from_numpy(oracle.rope_apply(q.double().numpy(), c, s)).to(torch.bfloat16)
-    kr = torch.from_numpy(oracle.rope_apply(k.double().numpy(), c, s)).to(torch.bfloat16)
+    c16 = c.astype(np.float16).astype(np.float64)
+    s16 = s.astype(np.float16).astype(np.float64)
+    qr = torch.from_numpy(oracle.rope_apply(q.double().numpy(), c16, s16)).to(torch.bfloat16)
+    kr = torch.from_numpy(oracle.rope_apply(k.double().numpy(), c16, s16)).to(torch.bfloat16)
     zero = np.zeros_like(ids)
     bound = MAX_ABS + 2.0 ** -8 * float(v.float().abs().max())
     _compare(out, qr, kr, v, zero[:33], zero[33:], max_abs=bound)
