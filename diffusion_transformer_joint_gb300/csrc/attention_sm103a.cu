@@ -338,17 +338,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       tmem_ld_wait();
       const int valid = static_cast<int>(S - static_cast<int64_t>(j) * kBN);
-      float mx = -INFINITY;
-      if (valid >= kBN) {
+      if (valid < kBN) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
-      } else {
-#pragma unroll
-        for (int i = 0; i < kBN; ++i) {
+        for (int i = 0; i < kBN; ++i)
           if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
-          mx = fmaxf(mx, __uint_as_float(sr[i]));
-        }
       }
+      // row max: four independent chains of 3-input max
+      float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kBN; i += 8) {
+        ma = fmax3(ma, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+        mb = fmax3(mb, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+        mc = fmax3(mc, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+        md = fmax3(md, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+      }
+      float mx = fmax3(ma, mb, fmaxf(mc, md));
       mx *= scale_log2;
       float alpha = 1.f;
       float m_use = m_run;
@@ -368,20 +372,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st16(tO + c * 16, o);
         }
       }
-      const float neg_m = -m_use;
-      float sum = 0.f;
-      // P in four chunks of 32 keys (16 packed columns each) to bound registers
+      // p = 2^(s * scale - m): scale and shift on fp32 pairs, exp2 per lane,
+      // row sum in four pair accumulators, P packed to bf16 in four chunks of
+      // 32 keys (16 TMEM columns each) to bound registers.
+      const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+      const uint64_t negm2 = f2_pack(-m_use, -m_use);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c * 32 + i]), scale_log2, neg_m));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c * 32 + i + 1]), scale_log2, neg_m));
-          sum += p0 + p1;
+          const uint64_t x2 = f2_pack(__uint_as_float(sr[c * 32 + i]), __uint_as_float(sr[c * 32 + i + 1]));
+          float y0, y1;
+          f2_unpack(f2_fma(x2, scale2, negm2), y0, y1);
+          const float p0 = ex2_approx(y0);
+          const float p1 = ex2_approx(y1);
+          acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
           pk[i / 2] = pack_bf16x2(p0, p1);
         }
         tmem_st16(tS + c * 16, pk);
+      }
+      float sum;
+      {
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+        sum = (a0 + a1) + (b0 + b1);
       }
       tmem_st_wait();
       l_run = l_run * alpha + sum;
