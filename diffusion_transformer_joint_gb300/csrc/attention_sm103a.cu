@@ -8,8 +8,12 @@
 //   out[b, i, h, :] = sum_j softmax_j(q^_i . k^_j / sqrt(128)) v[b, j, h, :]
 // with q^, k^ the RoPE-rotated rows; non-causal over all S tokens.
 //
-// One CTA owns 256 query rows (two 128-row tiles Q0, Q1) of one (batch, head)
-// and walks every 128-key tile. 16 warps in four warpgroups:
+// Persistent: one CTA per SM walks work items (batch, head, 256-row block)
+// round robin; for each it owns 256 query rows (two 128-row tiles Q0, Q1)
+// and walks every 128-key tile. The K/V rings, the table ring and every
+// barrier phase run on across items, so the next item's Q is loaded and
+// rotated while the current item's last tiles and epilogue finish.
+// 16 warps in four warpgroups:
 //   WG0  warp 0: TMA producer of raw Q (once), raw K tiles (2-stage ring) and
 //        the packed (cos, sin) table in 64-token halves (2-buffer ring);
 //        warp 1: MMA issuer (one thread); warp 2: TMEM allocation;
@@ -82,7 +86,9 @@ constexpr int kBarTEmpty = kBarTFull + 2;
 constexpr int kBarSFull = kBarTEmpty + 2;  // + q tile
 constexpr int kBarPFull = kBarSFull + kQTiles;
 constexpr int kBarODone = kBarPFull + kQTiles;
-constexpr int kBarDrain = kBarODone + kQTiles;
+constexpr int kBarOFree = kBarODone + kQTiles;  // epilogue done reading O_t
+constexpr int kBarQFree = kBarOFree + kQTiles;  // every S MMA of an item done
+constexpr int kBarDrain = kBarQFree + 1;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
@@ -91,8 +97,8 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
-constexpr uint32_t kRegsSoftmax = 168;
-constexpr uint32_t kRegsOther = 88;
+constexpr uint32_t kRegsSoftmax = 160;
+constexpr uint32_t kRegsOther = 96;
 static_assert(128 * (2 * kRegsSoftmax + 2 * kRegsOther) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -156,7 +162,7 @@ struct Maps {
 
 __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
-                                int *__restrict__ status, int64_t S, int H) {
+                                int *__restrict__ status, int64_t S, int H, int n_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -169,12 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int m0 = static_cast<int>(blockIdx.x) * kRowsPerCta;
-  const int h = static_cast<int>(blockIdx.y);
-  const int b = static_cast<int>(blockIdx.z);
   const int64_t row_stride = static_cast<int64_t>(H) * kD;
-  const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;
   const int n_tiles = static_cast<int>((S + kBN - 1) / kBN);
+  const int n_rb = static_cast<int>((S + kRowsPerCta - 1) / kRowsPerCta);  // row blocks per head
+  // Work items (batch, head, row block), row block fastest, handed out round
+  // robin: CTAs running at the same time share the K/V of a few heads in L2.
+  auto decode = [&](int item, int &b, int &h, int &m0) {
+    m0 = (item % n_rb) * kRowsPerCta;
+    const int bh = item / n_rb;
+    h = bh % H;
+    b = bh / H;
+  };
 
   if (tid == 0) {
     mbar_init(bar(kBarQRaw), 1);
@@ -194,7 +205,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarSFull + t), 1);
       mbar_init(bar(kBarPFull + t), 128);
       mbar_init(bar(kBarODone + t), 1);
+      mbar_init(bar(kBarOFree + t), 128);
     }
+    mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -218,13 +231,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.table);
-      mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
-      for (int t = 0; t < kQTiles; ++t) {
-        const uint32_t dst = sbase + kOffQ + t * kTileBytes;
-        tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
-        tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
-      }
-      int g = 0;  // table halves issued so far
+      int g = 0;   // table halves issued so far
+      int jt = 0;  // K tiles issued so far (all items)
       bool ok = true;
       auto table_half = [&](int row0) {
         const int buf = g & 1;
@@ -235,81 +243,115 @@ __global__ void __launch_bounds__(kThreads, 1)
                     row0);
         ++g;
       };
-      for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t use = static_cast<uint32_t>(j / kStages);
-        if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
-        const uint32_t dst = sbase + kOffK + s * kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
-        tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, j * kBN, b);
-        tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, j * kBN, b);
-        table_half(j * kBN);
-        if (ok) table_half(j * kBN + static_cast<int>(kHalfRows));
+      int k = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        int b, h, m0;
+        decode(item, b, h, m0);
+        // the previous item's S MMAs no longer read the Q buffers
+        if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
+          break;
+        mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
+        for (int t = 0; t < kQTiles; ++t) {
+          const uint32_t dst = sbase + kOffQ + t * kTileBytes;
+          tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
+          tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
+        }
+        for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
+        for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
+          const int s = jt % kStages;
+          const uint32_t use = static_cast<uint32_t>(jt / kStages);
+          if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
+          const uint32_t dst = sbase + kOffK + s * kTileBytes;
+          mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
+          tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, j * kBN, b);
+          tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, j * kBN, b);
+          table_half(j * kBN);
+          if (ok) table_half(j * kBN + static_cast<int>(kHalfRows));
+        }
       }
     } else if (warp == 3 && lane == 0) {
       // ------------------------------------------------------ producer: V
       tma_prefetch_desc(&maps.v);
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t use = static_cast<uint32_t>(j / kStages);
-        if (!mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag)) break;
-        const uint32_t dst = sbase + kOffV + s * kTileBytes;
-        mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-        tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, j * kBN, b);
-        tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, j * kBN, b);
+      int jt = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+        int b, h, m0;
+        decode(item, b, h, m0);
+        for (int j = 0; j < n_tiles; ++j, ++jt) {
+          const int s = jt % kStages;
+          const uint32_t use = static_cast<uint32_t>(jt / kStages);
+          if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
+          const uint32_t dst = sbase + kOffV + s * kTileBytes;
+          mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
+          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, j * kBN, b);
+          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, j * kBN, b);
+        }
       }
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------ MMA issuer
       // TMEM: S_t at column 128 t, O_t at 256 + 128 t; Q_t at kOffQ + t * kTileBytes
-      bool ok = mbar_wait(bar(kBarQFull), 0, abort_flag);
-      ok = ok && mbar_wait(bar(kBarKFull + 0), 0, abort_flag);
-      if (ok) {
-        tc_fence_after_sync();
-        const uint32_t sK = sbase + kOffK;
+      auto issue_s = [&](int t, uint32_t sK) {
 #pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-#pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk)
-            mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
-                   desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
-          mma_commit(bar(kBarSFull + t));
-        }
-        mma_commit(bar(kBarKEmpty + 0));
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int sv = j % kStages;
-        const uint32_t sV = sbase + kOffV + sv * kTileBytes;
-        const bool more = j + 1 < n_tiles;
-        const int sk = (j + 1) % kStages;
-        const uint32_t sK = sbase + kOffK + sk * kTileBytes;
-        if (!(ok = mbar_wait(bar(kBarVFull + sv), static_cast<uint32_t>(j / kStages) & 1u,
-                             abort_flag)))
-          break;
-#pragma unroll
-        for (int t = 0; t < kQTiles; ++t) {
-          if (!(ok = mbar_wait(bar(kBarPFull + t), static_cast<uint32_t>(j) & 1u, abort_flag))) break;
+        for (int kk = 0; kk < kD / 16; ++kk)
+          mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
+                 desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
+        mma_commit(bar(kBarSFull + t));
+      };
+      int jt = 0;  // first global K/V tile index of the current item
+      bool ok = true;
+      int k = 0;
+      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        if (!(ok = mbar_wait(bar(kBarQFull), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
+        {
+          const int s0 = jt % kStages;
+          if (!(ok = mbar_wait(bar(kBarKFull + s0), static_cast<uint32_t>(jt / kStages) & 1u,
+                               abort_flag)))
+            break;
           tc_fence_after_sync();
+          for (int t = 0; t < kQTiles; ++t) issue_s(t, sbase + kOffK + s0 * kTileBytes);
+          mma_commit(bar(kBarKEmpty + s0));
+          if (n_tiles == 1) mma_commit(bar(kBarQFree));
+        }
+        for (int j = 0; ok && j < n_tiles; ++j) {
+          const int g0 = jt + j;  // global tile of this step
+          const int sv = g0 % kStages;
+          const uint32_t sV = sbase + kOffV + sv * kTileBytes;
+          const bool more = j + 1 < n_tiles;
+          const int sk = (g0 + 1) % kStages;
+          const uint32_t sK = sbase + kOffK + sk * kTileBytes;
+          if (!(ok = mbar_wait(bar(kBarVFull + sv), static_cast<uint32_t>(g0 / kStages) & 1u,
+                               abort_flag)))
+            break;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_v(sV, kk), idesc_pv,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(bar(kBarODone + t));
-          if (t == kQTiles - 1) mma_commit(bar(kBarVEmpty + sv));
-          if (more) {
-            if (t == 0 &&
-                !(ok = mbar_wait(bar(kBarKFull + sk), static_cast<uint32_t>((j + 1) / kStages) & 1u,
-                                 abort_flag)))
+          for (int t = 0; t < kQTiles; ++t) {
+            if (!(ok = mbar_wait(bar(kBarPFull + t), static_cast<uint32_t>(g0) & 1u, abort_flag)))
+              break;
+            // the previous item's epilogue has read O_t before it is overwritten
+            if (j == 0 && k > 0 &&
+                !(ok = mbar_wait(bar(kBarOFree + t), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
               break;
             tc_fence_after_sync();
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk)
-              mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
-                     desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
-            mma_commit(bar(kBarSFull + t));
-            if (t == kQTiles - 1) mma_commit(bar(kBarKEmpty + sk));
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_v(sV, kk), idesc_pv,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(bar(kBarODone + t));
+            if (t == kQTiles - 1) mma_commit(bar(kBarVEmpty + sv));
+            if (more) {
+              if (t == 0 &&
+                  !(ok = mbar_wait(bar(kBarKFull + sk), static_cast<uint32_t>((g0 + 1) / kStages) & 1u,
+                                   abort_flag)))
+                break;
+              tc_fence_after_sync();
+              issue_s(t, sK);
+              if (t == kQTiles - 1) {
+                mma_commit(bar(kBarKEmpty + sk));
+                if (j + 2 == n_tiles) mma_commit(bar(kBarQFree));  // last S of the item
+              }
+            }
           }
         }
+        jt += n_tiles;
       }
       // drain: every MMA issued above has finished before TMEM is released
       mma_commit(bar(kBarDrain));
@@ -327,89 +369,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * 128 + lane_off;
     const float scale_log2 = 1.4426950408889634f * 0.08838834764831845f;
-    float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!(ok = mbar_wait(bar(kBarSFull + t), static_cast<uint32_t>(j) & 1u, abort_flag))) break;
-      tc_fence_after_sync();
-      uint32_t sr[kBN];
+    int jt = 0;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < n_tiles; ++j, ++jt) {
+        if (!(ok = mbar_wait(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
+        tc_fence_after_sync();
+        uint32_t sr[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_ld_wait();
-      const int valid = static_cast<int>(S - static_cast<int64_t>(j) * kBN);
-      if (valid < kBN) {
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_ld_wait();
+        const int valid = static_cast<int>(S - static_cast<int64_t>(j) * kBN);
+        if (valid < kBN) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
-          if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
-      }
-      // row max: four independent chains of 3-input max
-      float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+          for (int i = 0; i < kBN; ++i)
+            if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
+        }
+        // row max: four independent chains of 3-input max
+        float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < kBN; i += 8) {
-        ma = fmax3(ma, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-        mb = fmax3(mb, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-        mc = fmax3(mc, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-        md = fmax3(md, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
-      }
-      float mx = fmax3(ma, mb, fmaxf(mc, md));
-      mx *= scale_log2;
-      float alpha = 1.f;
-      float m_use = m_run;
-      if (j == 0) {
-        m_use = mx;
-      } else if (__any_sync(0xffffffffu, mx > m_run + kRescaleThreshold)) {
-        m_use = fmaxf(m_run, mx);
-        alpha = ex2_approx(m_run - m_use);
-        // S_t(j) is complete, hence so is PV_t(j-1): O_t is stable here.
+        for (int i = 0; i < kBN; i += 8) {
+          ma = fmax3(ma, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+          mb = fmax3(mb, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+          mc = fmax3(mc, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+          md = fmax3(md, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+        }
+        float mx = fmax3(ma, mb, fmaxf(mc, md));
+        mx *= scale_log2;
+        float alpha = 1.f;
+        float m_use = m_run;
+        if (j == 0) {
+          m_use = mx;
+        } else if (__any_sync(0xffffffffu, mx > m_run + kRescaleThreshold)) {
+          m_use = fmaxf(m_run, mx);
+          alpha = ex2_approx(m_run - m_use);
+          // S_t(j) is complete, hence so is PV_t(j-1): O_t is stable here.
 #pragma unroll 1
-        for (int c = 0; c < kD / 16; ++c) {
-          uint32_t o[16];
-          tmem_ld16(tO + c * 16, o);
-          tmem_ld_wait();
+          for (int c = 0; c < kD / 16; ++c) {
+            uint32_t o[16];
+            tmem_ld16(tO + c * 16, o);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st16(tO + c * 16, o);
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + c * 16, o);
+          }
         }
-      }
-      // p = 2^(s * scale - m): scale and shift on fp32 pairs, exp2 per lane,
-      // row sum in four pair accumulators, P packed to bf16 in four chunks of
-      // 32 keys (16 TMEM columns each) to bound registers.
-      const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
-      const uint64_t negm2 = f2_pack(-m_use, -m_use);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+        // p = 2^(s * scale - m): scale and shift on fp32 pairs, exp2 per lane,
+        // row sum in four pair accumulators, P packed to bf16 in four chunks of
+        // 32 keys (16 TMEM columns each) to bound registers.
+        const uint64_t scale2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t negm2 = f2_pack(-m_use, -m_use);
+        uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          const uint64_t x2 = f2_pack(__uint_as_float(sr[c * 32 + i]), __uint_as_float(sr[c * 32 + i + 1]));
-          float y0, y1;
-          f2_unpack(f2_fma(x2, scale2, negm2), y0, y1);
-          const float p0 = ex2_approx(y0);
-          const float p1 = ex2_approx(y1);
-          acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
-          pk[i / 2] = pack_bf16x2(p0, p1);
+          for (int i = 0; i < 32; i += 2) {
+            const uint64_t x2 =
+                f2_pack(__uint_as_float(sr[c * 32 + i]), __uint_as_float(sr[c * 32 + i + 1]));
+            float y0, y1;
+            f2_unpack(f2_fma(x2, scale2, negm2), y0, y1);
+            const float p0 = ex2_approx(y0);
+            const float p1 = ex2_approx(y1);
+            acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
+            pk[i / 2] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(tS + c * 16, pk);
         }
-        tmem_st16(tS + c * 16, pk);
+        float sum;
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
+          f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
+          sum = (a0 + a1) + (b0 + b1);
+        }
+        tmem_st_wait();
+        l_run = l_run * alpha + sum;
+        m_run = m_use;
+        tc_fence_before_sync();
+        mbar_arrive(bar(kBarPFull + t));
       }
-      float sum;
-      {
-        float a0, a1, b0, b1;
-        f2_unpack(f2_add(acc[0], acc[1]), a0, a1);
-        f2_unpack(f2_add(acc[2], acc[3]), b0, b1);
-        sum = (a0 + a1) + (b0 + b1);
-      }
-      tmem_st_wait();
-      l_run = l_run * alpha + sum;
-      m_run = m_use;
-      tc_fence_before_sync();
-      mbar_arrive(bar(kBarPFull + t));
-    }
-    if (ok && mbar_wait(bar(kBarODone + t), static_cast<uint32_t>(n_tiles - 1) & 1u, abort_flag)) {
+      if (!ok) break;
+      // epilogue: wait for the item's last P V, normalise, store bf16 rows
+      if (!(ok = mbar_wait(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
       tc_fence_after_sync();
+      int b, h, m0;
+      decode(item, b, h, m0);
       const float inv_l = 1.f / l_run;
       const int64_t token = static_cast<int64_t>(m0) + t * kBM + row;
+      const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;
       uint16_t *orow = out + head0 + token * row_stride;
 #pragma unroll
       for (int c = 0; c < kD / 32; ++c) {
@@ -428,13 +478,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      tc_fence_before_sync();
+      mbar_arrive(bar(kBarOFree + t));
     }
   } else {
     // --------------------------------------------------------- RoPE warps
     reg_dec<kRegsOther>();
     const int u = tid - 384;
-    int g = 0;  // table halves consumed so far
-    bool ok = mbar_wait(bar(kBarQRaw), 0, abort_flag);
+    int g = 0;   // table halves consumed so far
+    int jt = 0;  // K tiles consumed so far
+    bool ok = true;
     auto rotate_tile = [&](uint32_t tile) {
       for (int half = 0; ok && half < 2; ++half) {
         const int buf = g & 1;
@@ -445,19 +498,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
     };
-    for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes);
-    if (ok) {
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kBarQFull));
-    }
-    for (int j = 0; ok && j < n_tiles; ++j) {
-      const int s = j % kStages;
-      if (!(ok = mbar_wait(bar(kBarKRaw + s), static_cast<uint32_t>(j / kStages) & 1u, abort_flag)))
-        break;
-      rotate_tile(sbase + kOffK + s * kTileBytes);
+    int k = 0;
+    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+      if (!(ok = mbar_wait(bar(kBarQRaw), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
+      for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes);
       if (!ok) break;
       fence_proxy_async_smem();
-      mbar_arrive(bar(kBarKFull + s));
+      mbar_arrive(bar(kBarQFull));
+      for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
+        const int s = jt % kStages;
+        if (!(ok = mbar_wait(bar(kBarKRaw + s), static_cast<uint32_t>(jt / kStages) & 1u,
+                             abort_flag)))
+          break;
+        rotate_tile(sbase + kOffK + s * kTileBytes);
+        if (!ok) break;
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarKFull + s));
+      }
     }
   }
 
@@ -541,10 +598,19 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
       !make_head_map(&maps.v, v, B, S, H) || !make_table_map(&maps.table, table, S))
     return cudaErrorInvalidValue;
-  const dim3 grid(static_cast<unsigned>((S + kRowsPerCta - 1) / kRowsPerCta),
-                  static_cast<unsigned>(H), static_cast<unsigned>(B));
+  // persistent: one CTA per SM, work items handed out round robin
+  static int sm_count[64];
+  if (sm_count[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    sm_count[dev] = n;
+  }
+  const int64_t items = static_cast<int64_t>(B) * H * ((S + kRowsPerCta - 1) / kRowsPerCta);
+  if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
   joint_rope_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      maps, static_cast<uint16_t *>(out), status, S, H);
+      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items));
   return cudaGetLastError();
 }
 
