@@ -14,14 +14,14 @@ namespace flux {
 constexpr int kMaxPairs = 256;
 
 // Per-pair RoPE parameters handed to the table kernel by value: the axis a
-// pair belongs to, its index j inside the axis and the axis width d_a.
+// pair belongs to, and its frequency in turns per unit of position id,
+// theta^(-2j/d_a) / (2 pi) (j the pair's index inside its axis of width
+// d_a), as an unsigned 0.64 fixed-point fraction of a turn (it is < 1).
 struct RopePairs {
   int n_pairs;
   int n_axes;
-  double theta;
   uint8_t axis[kMaxPairs];
-  uint8_t j[kMaxPairs];
-  uint16_t d_axis[kMaxPairs];
+  uint64_t turns_q64[kMaxPairs];
 };
 
 // Fills `pp` from host axes_dims; returns FLUX_OK or FLUX_ERR_AXES.

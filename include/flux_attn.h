@@ -69,8 +69,11 @@ typedef enum {
  * and j = p - o_a:
  *     angle(s, p) = ids[s, a] * theta^(-2 j / axes_dims[a])
  *     cos_out[s, p] = cos(angle),  sin_out[s, p] = sin(angle)
- * The angle is formed in double precision and reduced to [-pi, pi] before the
- * fp32 cosine and sine, so any int32 id value is accurate to ~2e-7.
+ * The frequency theta^(-2j/d_a) / (2 pi) turns per unit id is formed on the
+ * host in extended precision as a 0.64 fixed-point fraction; per entry the
+ * angle's fractional turn is the exact 64-bit product id * frequency
+ * (mod 2^64), and cosine and sine of it are evaluated in fp32, so outputs are
+ * accurate to a few 1e-7 for any int32 id.
  *
  *   ids        device, int32 [S, n_axes] row-major (one row per token).
  *   S          number of tokens, 1 <= S <= 2^31 - 1.
