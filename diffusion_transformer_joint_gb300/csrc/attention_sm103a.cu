@@ -160,6 +160,15 @@ struct Maps {
   CUtensorMap q, k, v, table;
 };
 
+// After an abort: wait (bounded, regardless of the abort flag) until the
+// phase of a TMA barrier completes, so that no copy this thread issued is
+// still in flight when the CTA exits.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitBudgetCycles) {
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
                                 int *__restrict__ status, int64_t S, int H, int n_items) {
@@ -244,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       };
       int k = 0;
+      int q_loads = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
         int b, h, m0;
         decode(item, b, h, m0);
         // the previous item's S MMAs no longer read the Q buffers
         if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
           break;
+        ++q_loads;
         mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
         for (int t = 0; t < kQTiles; ++t) {
           const uint32_t dst = sbase + kOffQ + t * kTileBytes;
@@ -269,6 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) table_half(j * kBN + static_cast<int>(kHalfRows));
         }
       }
+      {  // every copy issued above has landed before the CTA exits (a no-op
+         // unless an abort left some unconsumed)
+        if (q_loads > 0) drain_wait(bar(kBarQRaw), static_cast<uint32_t>(q_loads - 1) & 1u);
+        for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj)
+          drain_wait(bar(kBarKRaw + jj % kStages), static_cast<uint32_t>(jj / kStages) & 1u);
+        for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
+          drain_wait(bar(kBarTFull + (gg & 1)), static_cast<uint32_t>(gg >> 1) & 1u);
+      }
     } else if (warp == 3 && lane == 0) {
       // ------------------------------------------------------ producer: V
       tma_prefetch_desc(&maps.v);
@@ -287,6 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, j * kBN, b);
         }
       }
+      // every copy issued above has landed before the CTA exits (a no-op
+      // unless an abort left some unconsumed)
+      for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj)
+        drain_wait(bar(kBarVFull + jj % kStages), static_cast<uint32_t>(jj / kStages) & 1u);
     } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------ MMA issuer
       // TMEM: S_t at column 128 t, O_t at 256 + 128 t; Q_t at kOffQ + t * kTileBytes
