@@ -130,6 +130,30 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ------------------------------------------------- multi-rank host logic
+
+
+def rank_seed_offset(rank: int, set_index: int = 0) -> int:
+    """Seed offset of a rank's input set: every rank runs its own replica."""
+    return 100000 * rank + 17 * set_index
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's value (the whole job ends when it does)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(x)
+    import torch
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank_step: float, world: int, steps: int, t_max_ms: float) -> float:
+    """All ranks' FLOPs over the slowest rank's time (weak scaling)."""
+    return world * flops_per_rank_step * steps / (t_max_ms * 1e-3) / 1e12
+
+
 # ------------------------------------------------------------------ ours
 
 
@@ -160,7 +184,7 @@ def run_ours(args, rank, world, local_rank):
     n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
     sets = []
     for i in range(n_sets):
-        q, k, v = W.workload_qkv(w, seed_offset=100000 * rank + 17 * i)
+        q, k, v = W.workload_qkv(w, seed_offset=rank_seed_offset(rank, i))
         sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
     P = w.D // 2
     table = torch.empty((w.S, P), dtype=torch.int32, device=dev)
@@ -203,24 +227,17 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st} after the timed steps")
 
-    t_max = total_ms
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = max_over_ranks(total_ms, dist, dev)
 
     # end-to-end through the public one-call API with host buffers
     e2e = run_e2e(w, dev, K, args.warmup, binding, W, torch, np, txt_np, img_np)
-    if dist is not None:
-        e = torch.tensor([e2e["ms_per_step"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(e, op=dist.ReduceOp.MAX)
-        e2e["ms_per_step"] = float(e.item())
+    e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dist, dev)
 
     if rank != 0:
         return None
     peaks, peak_src = _peaks()
     flops_step = w.flops
-    value = world * flops_step * K / (t_max * 1e-3) / 1e12
+    value = whole_job_tflops(flops_step, world, K, t_max)
     attn_avg_ms = statistics.mean(attn_ms)
     achieved = flops_step / (attn_avg_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -264,7 +281,7 @@ def run_ours(args, rank, world, local_rank):
             "avg_launch_ms": round(attn_avg_ms, 4),
         },
         "clocks": clocks.summary(),
-        "e2e": {"value": round(world * flops_step / (e2e["ms_per_step"] * 1e-3) / 1e12, 2),
+        "e2e": {"value": round(whole_job_tflops(flops_step, world, 1, e2e["ms_per_step"]), 2),
                 "unit": UNIT, "ms_per_step": round(e2e["ms_per_step"], 4),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "api": "flux_joint_rope_attention (one call: tables + attention)"},
