@@ -160,6 +160,25 @@ struct Maps {
   CUtensorMap q, k, v, table;
 };
 
+// mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
+// lanes agree on the outcome, so an abort never splits a warp between a
+// warp-collective instruction (tcgen05.ld/st, __syncwarp) and the exit path.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
+                                               volatile int *abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
+}
+
+// One arrival per warp on a hand-off barrier (initialised with the number of
+// arriving warps): every lane has finished its part (its smem writes fenced
+// for the async proxy, its TMEM stores waited and fenced) before __syncwarp,
+// then lane 0 arrives for the warp. Four arrivals instead of 128 shorten the
+// hand-off.
+__device__ __forceinline__ void warp_arrive(uint32_t bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
 // After an abort: wait (bounded, regardless of the abort flag) until the
 // phase of a TMA barrier completes, so that no copy this thread issued is
 // still in flight when the CTA exits.
@@ -198,23 +217,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(bar(kBarQRaw), 1);
-    mbar_init(bar(kBarQFull), 128);
+    mbar_init(bar(kBarQFull), 4);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKRaw + s), 1);
-      mbar_init(bar(kBarKFull + s), 128);
+      mbar_init(bar(kBarKFull + s), 4);
       mbar_init(bar(kBarKEmpty + s), 1);
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(kBarTFull + i), 1);
-      mbar_init(bar(kBarTEmpty + i), 128);
+      mbar_init(bar(kBarTEmpty + i), 4);
     }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
-      mbar_init(bar(kBarPFull + t), 128);
+      mbar_init(bar(kBarPFull + t), 4);
       mbar_init(bar(kBarODone + t), 1);
-      mbar_init(bar(kBarOFree + t), 128);
+      mbar_init(bar(kBarOFree + t), 4);
     }
     mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarDrain), 1);
@@ -397,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++jt) {
-        if (!(ok = mbar_wait(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
         tc_fence_after_sync();
         uint32_t sr[kBN];
 #pragma unroll
@@ -472,11 +491,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_run = l_run * alpha + sum;
         m_run = m_use;
         tc_fence_before_sync();
-        mbar_arrive(bar(kBarPFull + t));
+        warp_arrive(bar(kBarPFull + t), lane);
       }
       if (!ok) break;
       // epilogue: wait for the item's last P V, normalise, store bf16 rows
-      if (!(ok = mbar_wait(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
       tc_fence_after_sync();
       int b, h, m0;
       decode(item, b, h, m0);
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before_sync();
-      mbar_arrive(bar(kBarOFree + t));
+      warp_arrive(bar(kBarOFree + t), lane);
     }
   } else {
     // --------------------------------------------------------- RoPE warps
@@ -514,29 +533,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto rotate_tile = [&](uint32_t tile) {
       for (int half = 0; ok && half < 2; ++half) {
         const int buf = g & 1;
-        if (!(ok = mbar_wait(bar(kBarTFull + buf), static_cast<uint32_t>(g >> 1) & 1u, abort_flag)))
+        if (!(ok = mbar_wait_warp(bar(kBarTFull + buf), static_cast<uint32_t>(g >> 1) & 1u, abort_flag)))
           return;
         rotate_half(tile, sbase + kOffT + buf * kTableHalfBytes, half, u);
-        mbar_arrive(bar(kBarTEmpty + buf));
+        warp_arrive(bar(kBarTEmpty + buf), lane);
         ++g;
       }
     };
     int k = 0;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
-      if (!(ok = mbar_wait(bar(kBarQRaw), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(bar(kBarQRaw), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
       for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes);
       if (!ok) break;
       fence_proxy_async_smem();
-      mbar_arrive(bar(kBarQFull));
+      warp_arrive(bar(kBarQFull), lane);
       for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
         const int s = jt % kStages;
-        if (!(ok = mbar_wait(bar(kBarKRaw + s), static_cast<uint32_t>(jt / kStages) & 1u,
+        if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), static_cast<uint32_t>(jt / kStages) & 1u,
                              abort_flag)))
           break;
         rotate_tile(sbase + kOffK + s * kTileBytes);
         if (!ok) break;
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarKFull + s));
+        warp_arrive(bar(kBarKFull + s), lane);
       }
     }
   }

@@ -25,8 +25,8 @@ from diffusion_transformer_joint_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-ANCHOR = "mbar_arrive(bar(kBarKFull + s));"
-WITHHELD = "if (jt != 0) mbar_arrive(bar(kBarKFull + s));"
+ANCHOR = "warp_arrive(bar(kBarKFull + s), lane);"
+WITHHELD = "if (jt != 0) warp_arrive(bar(kBarKFull + s), lane);"
 
 
 def _build_withholding_library(tmp_path):
