@@ -329,66 +329,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       // unless an abort left some unconsumed)
       for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj)
         drain_wait(bar(kBarVFull + jj % kStages), static_cast<uint32_t>(jj / kStages) & 1u);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ------------------------------------------------------ MMA issuer
+      // The whole warp walks the schedule (its waits are warp-collective);
+      // elect.sync picks the lane that issues each tcgen05 instruction.
       // TMEM: S_t at column 128 t, O_t at 256 + 128 t; Q_t at kOffQ + t * kTileBytes
-      auto issue_s = [&](int t, uint32_t sK) {
+      const uint64_t dq0 = desc_kmajor(sbase + kOffQ, 0);
+      const uint64_t dk0 = desc_kmajor(sbase + kOffK, 0);
+      const uint64_t dv0 = desc_v(sbase + kOffV, 0);
+      auto issue_s = [&](int t, int sk) {
+        const uint64_t da = desc_advance(dq0, t * kTileBytes);
+        const uint64_t db = desc_advance(dk0, sk * kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk)
-          mma_ss(tmem + t * 128, desc_kmajor(sbase + kOffQ + t * kTileBytes, kk),
-                 desc_kmajor(sK, kk), idesc_qk, kk > 0 ? 1u : 0u);
-        mma_commit(bar(kBarSFull + t));
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
+          mma_ss_elect(tmem + t * 128, desc_advance(da, off), desc_advance(db, off), idesc_qk,
+                       kk > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(bar(kBarSFull + t));
       };
       int jt = 0;  // first global K/V tile index of the current item
       bool ok = true;
       int k = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
-        if (!(ok = mbar_wait(bar(kBarQFull), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar(kBarQFull), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
         {
           const int s0 = jt % kStages;
-          if (!(ok = mbar_wait(bar(kBarKFull + s0), static_cast<uint32_t>(jt / kStages) & 1u,
-                               abort_flag)))
+          if (!(ok = mbar_wait_warp(bar(kBarKFull + s0), static_cast<uint32_t>(jt / kStages) & 1u,
+                                    abort_flag)))
             break;
           tc_fence_after_sync();
-          for (int t = 0; t < kQTiles; ++t) issue_s(t, sbase + kOffK + s0 * kTileBytes);
-          mma_commit(bar(kBarKEmpty + s0));
-          if (n_tiles == 1) mma_commit(bar(kBarQFree));
+          for (int t = 0; t < kQTiles; ++t) issue_s(t, s0);
+          mma_commit_elect(bar(kBarKEmpty + s0));
+          if (n_tiles == 1) mma_commit_elect(bar(kBarQFree));
         }
         for (int j = 0; ok && j < n_tiles; ++j) {
           const int g0 = jt + j;  // global tile of this step
           const int sv = g0 % kStages;
-          const uint32_t sV = sbase + kOffV + sv * kTileBytes;
+          const uint64_t dv = desc_advance(dv0, sv * kTileBytes);
           const bool more = j + 1 < n_tiles;
           const int sk = (g0 + 1) % kStages;
-          const uint32_t sK = sbase + kOffK + sk * kTileBytes;
-          if (!(ok = mbar_wait(bar(kBarVFull + sv), static_cast<uint32_t>(g0 / kStages) & 1u,
-                               abort_flag)))
+          if (!(ok = mbar_wait_warp(bar(kBarVFull + sv), static_cast<uint32_t>(g0 / kStages) & 1u,
+                                    abort_flag)))
             break;
-#pragma unroll
+#pragma unroll 1
           for (int t = 0; t < kQTiles; ++t) {
-            if (!(ok = mbar_wait(bar(kBarPFull + t), static_cast<uint32_t>(g0) & 1u, abort_flag)))
+            if (!(ok = mbar_wait_warp(bar(kBarPFull + t), static_cast<uint32_t>(g0) & 1u, abort_flag)))
               break;
             // the previous item's epilogue has read O_t before it is overwritten
             if (j == 0 && k > 0 &&
-                !(ok = mbar_wait(bar(kBarOFree + t), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
+                !(ok = mbar_wait_warp(bar(kBarOFree + t), static_cast<uint32_t>(k - 1) & 1u,
+                                      abort_flag)))
               break;
             tc_fence_after_sync();
 #pragma unroll
             for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_v(sV, kk), idesc_pv,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(bar(kBarODone + t));
-            if (t == kQTiles - 1) mma_commit(bar(kBarVEmpty + sv));
+              mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_advance(dv, kk * 2048),
+                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            mma_commit_elect(bar(kBarODone + t));
+            if (t == kQTiles - 1) mma_commit_elect(bar(kBarVEmpty + sv));
             if (more) {
               if (t == 0 &&
-                  !(ok = mbar_wait(bar(kBarKFull + sk), static_cast<uint32_t>((g0 + 1) / kStages) & 1u,
-                                   abort_flag)))
+                  !(ok = mbar_wait_warp(bar(kBarKFull + sk),
+                                        static_cast<uint32_t>((g0 + 1) / kStages) & 1u, abort_flag)))
                 break;
               tc_fence_after_sync();
-              issue_s(t, sK);
+              issue_s(t, sk);
               if (t == kQTiles - 1) {
-                mma_commit(bar(kBarKEmpty + sk));
-                if (j + 2 == n_tiles) mma_commit(bar(kBarQFree));  // last S of the item
+                mma_commit_elect(bar(kBarKEmpty + sk));
+                if (j + 2 == n_tiles) mma_commit_elect(bar(kBarQFree));  // last S of the item
               }
             }
           }
@@ -396,10 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         jt += n_tiles;
       }
       // drain: every MMA issued above has finished before TMEM is released
-      mma_commit(bar(kBarDrain));
+      mma_commit_elect(bar(kBarDrain));
       const long long t0 = clock64();
       while (!mbar_try_wait(bar(kBarDrain), 0) && clock64() - t0 < kWaitBudgetCycles) {
       }
+      __syncwarp();
     }
   } else if (warp < 12) {
     // ---------------------------------------------------------- softmax
