@@ -189,6 +189,7 @@ def run_ours(args, rank, world, local_rank):
     P = w.D // 2
     table = torch.empty((w.S, P), dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    krot = torch.empty(binding.krot_bytes(w.B, w.S, w.H, w.D), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, ev_mid=None):
@@ -196,7 +197,8 @@ def run_ours(args, rank, world, local_rank):
         binding.rope_tables_packed(ids, out=table, stream=stream)
         if ev_mid is not None:
             ev_mid.record(stream)
-        binding.joint_rope_attention_tabled(q, k, v, table, status, out=out, stream=stream)
+        binding.joint_rope_attention_tabled(q, k, v, table, status, out=out, stream=stream,
+                                            krot=krot)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -264,6 +266,8 @@ def run_ours(args, rank, world, local_rank):
             "l2": f"inputs rotate over {n_sets} sets of {set_bytes / 2**20:.0f} MiB "
                   f"({n_sets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
             "step": "rope_tables kernel + attention kernel (tables rebuilt every step)",
+            "k_rope": "rotated K tiles shared by the CTAs of a head through an exchange "
+                      f"buffer ({krot.numel() / 2**20:.0f} MiB)",
         },
         "pct_peak": round(100.0 * value / world / peak, 2),
         "roofline": {
@@ -304,7 +308,8 @@ def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
     dtxt = torch.empty_like(htxt, device=dev)
     dimg = torch.empty_like(himg, device=dev)
     dout = torch.empty_like(dq)
-    ws = torch.zeros(binding.workspace_bytes(w.S), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(binding.workspace_shared_bytes(w.B, w.S, w.H, w.D), dtype=torch.uint8,
+                     device=dev)
     stream = torch.cuda.Stream(device=dev)
 
     def one():

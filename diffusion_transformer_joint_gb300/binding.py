@@ -23,6 +23,7 @@ STATUS = {
 
 # every symbol include/flux_attn.h declares
 EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_attention_workspace",
+           "flux_joint_rope_attention_krot_bytes", "flux_joint_rope_attention_workspace_shared",
            "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
            "flux_query_status", "flux_status_string")
 
@@ -60,11 +61,15 @@ def load(path: str | None = None):
             lib.flux_rope_tables_packed.restype = I32
             lib.flux_joint_rope_attention_workspace.argtypes = [I64, I32]
             lib.flux_joint_rope_attention_workspace.restype = SZ
+            lib.flux_joint_rope_attention_krot_bytes.argtypes = [I32, I64, I32, I32]
+            lib.flux_joint_rope_attention_krot_bytes.restype = SZ
+            lib.flux_joint_rope_attention_workspace_shared.argtypes = [I32, I64, I32, I32]
+            lib.flux_joint_rope_attention_workspace_shared.restype = SZ
             lib.flux_joint_rope_attention.argtypes = [V, V, V, V, I64, V, I64, I32, I32, I32,
                                                       V, I32, D, V, V, SZ, V]
             lib.flux_joint_rope_attention.restype = I32
             lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, I32, I64, I32, I32, V,
-                                                             V, V]
+                                                             V, V, SZ, V]
             lib.flux_joint_rope_attention_tabled.restype = I32
             lib.flux_query_status.argtypes = [V, V]
             lib.flux_query_status.restype = I32
@@ -101,7 +106,18 @@ def _need_cuda(name, t, dtype):
 
 
 def workspace_bytes(S: int, D: int = 128) -> int:
+    """Smallest workspace of joint_rope_attention (status word + RoPE table)."""
     return int(load().flux_joint_rope_attention_workspace(int(S), int(D)))
+
+
+def krot_bytes(B: int, S: int, H: int, D: int = 128) -> int:
+    """Size of the rotated-K exchange buffer (0 for rejected shapes)."""
+    return int(load().flux_joint_rope_attention_krot_bytes(int(B), int(S), int(H), int(D)))
+
+
+def workspace_shared_bytes(B: int, S: int, H: int, D: int = 128) -> int:
+    """Workspace size with which joint_rope_attention shares rotated K tiles."""
+    return int(load().flux_joint_rope_attention_workspace_shared(int(B), int(S), int(H), int(D)))
 
 
 def rope_tables(ids, axes_dims=AXES_DIMS, theta=THETA, cos_out=None, sin_out=None, stream=None):
@@ -157,11 +173,13 @@ def unpack_table(packed):
 
 
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA, out=None,
-                         workspace=None, stream=None):
+                         workspace=None, stream=None, share_k=True):
     """softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v over the joint sequence [txt ; img].
 
     q, k, v: bf16 CUDA [B, S, H, 128]; txt_ids [S_txt, n_axes], img_ids
     [S_img, n_axes] int32 CUDA (either may be None / empty). Returns ``out``.
+    Without ``workspace`` one is allocated: with room for the rotated-K
+    exchange buffer when ``share_k``, else the smallest one.
     """
     import torch
 
@@ -179,8 +197,10 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
     else:
         _need_cuda("out", out, torch.bfloat16)
     if workspace is None:
-        workspace = torch.empty(max(workspace_bytes(max(S, 1), D), 256), dtype=torch.uint8,
-                                device=q.device)
+        n = workspace_shared_bytes(B, S, H, D) if share_k else 0
+        if n == 0:
+            n = workspace_bytes(max(S, 1), D)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     axes, n = _axes_array(axes_dims)
     rc = lib.flux_joint_rope_attention(
         _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes, n,
@@ -190,9 +210,11 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
     return out
 
 
-def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None):
+def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, krot=None):
     """Attention with a caller-built packed table (see rope_tables_packed); ``status``
-    is a device int32 tensor of one element that the caller clears."""
+    is a device int32 tensor of one element that the caller clears. ``krot``: a
+    uint8 CUDA tensor of at least krot_bytes(B, S, H) bytes serving as the
+    rotated-K exchange buffer; None allocates one, False runs without."""
     import torch
 
     lib = load()
@@ -203,8 +225,16 @@ def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None):
     B, S, H, D = q.shape
     if out is None:
         out = torch.empty_like(q)
+    if krot is None:
+        krot = torch.empty(max(krot_bytes(B, S, H, D), 256), dtype=torch.uint8, device=q.device)
+    if krot is False:
+        kp, kn = None, 0
+    else:
+        _need_cuda("krot", krot, torch.uint8)
+        kp, kn = _ptr(krot), krot.numel()
     rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H, D,
-                                              _ptr(out), _ptr(status), _stream_handle(stream))
+                                              _ptr(out), _ptr(status), kp, kn,
+                                              _stream_handle(stream))
     if rc != 0:
         raise FluxError("flux_joint_rope_attention_tabled", rc, lib)
     return out

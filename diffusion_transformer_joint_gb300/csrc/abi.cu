@@ -46,7 +46,7 @@ const char *flux_status_string(int status) {
     case FLUX_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case FLUX_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device timeout)";
     case FLUX_ERR_UNSUPPORTED: return "the current device is not sm_103 (GB300)";
-    case FLUX_ERR_ALIAS: return "out overlaps q, k or v";
+    case FLUX_ERR_ALIAS: return "out or a scratch buffer overlaps q, k, v or out";
     default: return "unknown status";
   }
 }
@@ -86,6 +86,15 @@ size_t flux_joint_rope_attention_workspace(int64_t S, int D) {
   if (S < 1 || S > 0x7FFFFFFFLL || D <= 0 || (D & 1)) return 0;
   return flux::kStatusBytes + flux::packed_table_bytes(S, D);
 }
+size_t flux_joint_rope_attention_krot_bytes(int B, int64_t S, int H, int D) {
+  if (B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535) return 0;
+  return flux::krot_scratch_bytes(B, S, H, D);
+}
+size_t flux_joint_rope_attention_workspace_shared(int B, int64_t S, int H, int D) {
+  const size_t base = flux_joint_rope_attention_workspace(S, D);
+  const size_t krot = flux_joint_rope_attention_krot_bytes(B, S, H, D);
+  return (base == 0 || krot == 0) ? 0 : base + krot;
+}
 
 int flux_joint_rope_attention(const void *q, const void *k, const void *v,
                               const int32_t *txt_ids, int64_t S_txt, const int32_t *img_ids,
@@ -114,6 +123,12 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < need)
     return FLUX_ERR_WORKSPACE;
+  // a workspace large enough for the rotated-K exchange buffer enables it
+  const size_t need_shared = flux_joint_rope_attention_workspace_shared(B, S, H, D);
+  const size_t used = (need_shared != 0 && workspace_bytes >= need_shared) ? need_shared : need;
+  if (overlaps(workspace, used, q, tensor_bytes) || overlaps(workspace, used, k, tensor_bytes) ||
+      overlaps(workspace, used, v, tensor_bytes) || overlaps(workspace, used, out, tensor_bytes))
+    return FLUX_ERR_ALIAS;
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
 
@@ -125,14 +140,16 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
   if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
                                nullptr, nullptr, table, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
-  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, st) != cudaSuccess)
+  void *krot = used == need ? nullptr : static_cast<void *>(ws + need);
+  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }
 
 int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
                                      const uint32_t *table, int B, int64_t S, int H, int D,
-                                     void *out, int32_t *status, void *stream) {
+                                     void *out, int32_t *status, void *krot_scratch,
+                                     size_t krot_bytes, void *stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || table == nullptr ||
       status == nullptr)
     return FLUX_ERR_NULL;
@@ -146,9 +163,19 @@ int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v
   if (overlaps(out, tensor_bytes, q, tensor_bytes) || overlaps(out, tensor_bytes, k, tensor_bytes) ||
       overlaps(out, tensor_bytes, v, tensor_bytes))
     return FLUX_ERR_ALIAS;
+  if (krot_scratch != nullptr) {
+    if ((reinterpret_cast<uintptr_t>(krot_scratch) & 255u) != 0 ||
+        krot_bytes < flux_joint_rope_attention_krot_bytes(B, S, H, D))
+      return FLUX_ERR_WORKSPACE;
+    const size_t kb = flux_joint_rope_attention_krot_bytes(B, S, H, D);
+    if (overlaps(krot_scratch, kb, q, tensor_bytes) || overlaps(krot_scratch, kb, k, tensor_bytes) ||
+        overlaps(krot_scratch, kb, v, tensor_bytes) ||
+        overlaps(krot_scratch, kb, out, tensor_bytes))
+      return FLUX_ERR_ALIAS;
+  }
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
-  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H,
+  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot_scratch,
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;

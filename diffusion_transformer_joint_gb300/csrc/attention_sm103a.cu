@@ -43,8 +43,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
+#include <random>
 
 #include "flux_internal.h"
 #include "ptx_sm103a.cuh"
@@ -66,6 +69,7 @@ constexpr uint32_t kHalfRows = 64;               // table rows per table buffer
 constexpr uint32_t kTableHalfBytes = kHalfRows * kPairs * 4;  // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kQPrefetchTiles = 6;  // key tiles before an item's end its successor's Q is prefetched
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;                                   // Q0, Q1
@@ -92,7 +96,8 @@ constexpr int kBarDrain = kBarQFree + 1;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kSmemUsed = kOffAbort + 4;
+constexpr uint32_t kOffKSrc = kOffAbort + 4;  // per K stage: 1 = landed already rotated
+constexpr uint32_t kSmemUsed = kOffKSrc + 4 * kStages;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
@@ -134,7 +139,13 @@ __device__ __forceinline__ void reg_dec() {
 // place with the table half at `tbl` ([64 rows][64 pairs] uint32). Thread u
 // owns 16-byte column chunk u & 15 (channel pairs 4(u&15) .. +3) of every
 // 8th row.
-__device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u) {
+// With kPublish, every rotated row whose token is below `rows_valid` (counted
+// from the tile's first row) is also stored to global memory at
+// grow + row * row_stride (bf16 elements, row 0 = the tile's first token).
+template <bool kPublish = false>
+__device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u,
+                                            uint16_t *grow = nullptr, int64_t row_stride = 0,
+                                            int rows_valid = 0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
   uint4 w[8], cs[8];
@@ -153,11 +164,13 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
     o.z = rope_pair(w[i].z, cs[i].z);
     o.w = rope_pair(w[i].w, cs[i].w);
     st_shared_v4(tile + sw128_offset(half * 64 + rh, c16), o);
+    if (kPublish && half * 64 + rh < rows_valid)
+      st_global_v4(grow + (half * 64 + rh) * row_stride + c16 * 8, o);
   }
 }
 
 struct Maps {
-  CUtensorMap q, k, v, table;
+  CUtensorMap q, k, v, table, krot;
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -190,7 +203,9 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 
 __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
-                                int *__restrict__ status, int64_t S, int H, int n_items) {
+                                int *__restrict__ status, int64_t S, int H, int n_items,
+                                uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
+                                uint64_t token) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -214,6 +229,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     h = bh % H;
     b = bh / H;
   };
+  // Key tiles are walked starting at a tile that depends on the row block,
+  // spread evenly over the head: the CTAs working on one head at the same
+  // time each rotate different K tiles first and publish them (kflags /
+  // krot), so that later each mostly loads tiles another CTA rotated.
+  auto first_tile = [&](int m0) {
+    return static_cast<int>((static_cast<int64_t>(m0 / kRowsPerCta) * n_tiles) / n_rb);
+  };
+  auto tile_at = [&](int j0, int j) { return j0 + j < n_tiles ? j0 + j : j0 + j - n_tiles; };
+  const bool share = kflags != nullptr;
 
   if (tid == 0) {
     mbar_init(bar(kBarQRaw), 1);
@@ -259,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.table);
+      if (share) tma_prefetch_desc(&maps.krot);
       int g = 0;   // table halves issued so far
       int jt = 0;  // K tiles issued so far (all items)
+      uint32_t rot_mask = 0;  // bit s: the last copy into K stage s was an already rotated tile
       bool ok = true;
       auto table_half = [&](int row0) {
         const int buf = g & 1;
@@ -287,23 +313,67 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
         }
         for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
+        const int j0 = first_tile(m0);
+        const uint64_t *fl_head =
+            share ? kflags + (static_cast<int64_t>(b) * H + h) * n_tiles * 4 : nullptr;
         for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
           const int s = jt % kStages;
+          const int tj = tile_at(j0, j);
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
+          // Has every RoPE warp of some CTA published tile tj? Decided (and
+          // the acquire fence paid) before the ring wait, which hides both.
+          bool rotated = false;
+          if (share) {
+            const uint64_t *fl = fl_head + static_cast<int64_t>(tj) * 4;
+            uint64_t f0, f1, f2, f3;
+            ld_relaxed_gpu_v2_u64(fl, f0, f1);
+            ld_relaxed_gpu_v2_u64(fl + 2, f2, f3);
+            rotated = f0 == token && f1 == token && f2 == token && f3 == token;
+            if (rotated) {
+              fence_acq_rel_gpu();         // acquire: the publishers' stores are visible
+              fence_proxy_async_global();  // to the TMA copy below as well
+            }
+          }
           if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
+          st_shared_u32(sbase + kOffKSrc + 4 * s, rotated ? 1u : 0u);
+          rot_mask = rotated ? (rot_mask | (1u << s)) : (rot_mask & ~(1u << s));
           const uint32_t dst = sbase + kOffK + s * kTileBytes;
-          mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
-          tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, j * kBN, b);
-          tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, j * kBN, b);
-          table_half(j * kBN);
-          if (ok) table_half(j * kBN + static_cast<int>(kHalfRows));
+          if (rotated) {
+            // straight to the MMA: the copy completes K-full, whose other
+            // three arrivals are made here; the RoPE warps only see K-raw
+            // complete and skip the tile
+            mbar_arrive(bar(kBarKRaw + s));
+            mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
+            tma_load_4d(dst, &maps.krot, bar(kBarKFull + s), 0, h, tj * kBN, b);
+            tma_load_4d(dst + kBlockBytes, &maps.krot, bar(kBarKFull + s), 64, h, tj * kBN, b);
+            mbar_arrive_n(bar(kBarKFull + s), 3);
+          } else {
+            mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
+            tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, tj * kBN, b);
+            tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, tj * kBN, b);
+            table_half(tj * kBN);
+            if (ok) table_half(tj * kBN + static_cast<int>(kHalfRows));
+          }
+          // the next item's Q into L2 a few tiles before it is loaded
+          if (j == (n_tiles > kQPrefetchTiles ? n_tiles - kQPrefetchTiles : 0) &&
+              item + static_cast<int>(gridDim.x) < n_items) {
+            int nb, nh, nm0;
+            decode(item + static_cast<int>(gridDim.x), nb, nh, nm0);
+            for (int t = 0; t < kQTiles && nm0 + t * kBM < S; ++t) {
+              tma_prefetch_l2_4d(&maps.q, 0, nh, nm0 + t * kBM, nb);
+              tma_prefetch_l2_4d(&maps.q, 64, nh, nm0 + t * kBM, nb);
+            }
+          }
         }
       }
       {  // every copy issued above has landed before the CTA exits (a no-op
          // unless an abort left some unconsumed)
         if (q_loads > 0) drain_wait(bar(kBarQRaw), static_cast<uint32_t>(q_loads - 1) & 1u);
-        for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj)
-          drain_wait(bar(kBarKRaw + jj % kStages), static_cast<uint32_t>(jj / kStages) & 1u);
+        for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj) {
+          const int sj = jj % kStages;  // a rotated tile's copy completes K-full
+          drain_wait(bar(((rot_mask >> sj) & 1u) ? kBarKFull + sj : kBarKRaw + sj),
+                     static_cast<uint32_t>(jj / kStages) & 1u);
+        }
         for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
           drain_wait(bar(kBarTFull + (gg & 1)), static_cast<uint32_t>(gg >> 1) & 1u);
       }
@@ -315,14 +385,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
         int b, h, m0;
         decode(item, b, h, m0);
+        const int j0 = first_tile(m0);
         for (int j = 0; j < n_tiles; ++j, ++jt) {
           const int s = jt % kStages;
+          const int tj = tile_at(j0, j);
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           const uint32_t dst = sbase + kOffV + s * kTileBytes;
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, j * kBN, b);
-          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, j * kBN, b);
+          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, tj * kBN, b);
+          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, tj * kBN, b);
         }
       }
       // every copy issued above has landed before the CTA exits (a no-op
@@ -424,6 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int jt = 0;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
+      int b, h, m0;
+      decode(item, b, h, m0);
+      const int j0 = first_tile(m0);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++jt) {
         if (!(ok = mbar_wait_warp(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
@@ -433,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN / 32; ++c)
           tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         tmem_ld_wait();
-        const int valid = static_cast<int>(S - static_cast<int64_t>(j) * kBN);
+        const int valid = static_cast<int>(S - static_cast<int64_t>(tile_at(j0, j)) * kBN);
         if (valid < kBN) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i)
@@ -507,8 +582,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: wait for the item's last P V, normalise, store bf16 rows
       if (!(ok = mbar_wait_warp(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
       tc_fence_after_sync();
-      int b, h, m0;
-      decode(item, b, h, m0);
       const float inv_l = 1.f / l_run;
       const int64_t token = static_cast<int64_t>(m0) + t * kBM + row;
       const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;
@@ -540,12 +613,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;   // table halves consumed so far
     int jt = 0;  // K tiles consumed so far
     bool ok = true;
-    auto rotate_tile = [&](uint32_t tile) {
+    // Rotates a landed tile in place; with `grow` (K tiles when sharing) the
+    // rotated rows also go to the exchange buffer.
+    auto rotate_tile = [&](uint32_t tile, uint16_t *grow, int rows_valid) {
       for (int half = 0; ok && half < 2; ++half) {
         const int buf = g & 1;
         if (!(ok = mbar_wait_warp(bar(kBarTFull + buf), static_cast<uint32_t>(g >> 1) & 1u, abort_flag)))
           return;
-        rotate_half(tile, sbase + kOffT + buf * kTableHalfBytes, half, u);
+        const uint32_t tbl = sbase + kOffT + buf * kTableHalfBytes;
+        if (grow != nullptr)
+          rotate_half<true>(tile, tbl, half, u, grow, row_stride, rows_valid);
+        else
+          rotate_half(tile, tbl, half, u);
         warp_arrive(bar(kBarTEmpty + buf), lane);
         ++g;
       }
@@ -553,19 +632,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     int k = 0;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
       if (!(ok = mbar_wait_warp(bar(kBarQRaw), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
-      for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes);
+      for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes, nullptr, 0);
       if (!ok) break;
       fence_proxy_async_smem();
       warp_arrive(bar(kBarQFull), lane);
+      int b, h, m0;
+      decode(item, b, h, m0);
+      const int j0 = first_tile(m0);
       for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
         const int s = jt % kStages;
         if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), static_cast<uint32_t>(jt / kStages) & 1u,
                              abort_flag)))
           break;
-        rotate_tile(sbase + kOffK + s * kTileBytes);
-        if (!ok) break;
-        fence_proxy_async_smem();
-        warp_arrive(bar(kBarKFull + s), lane);
+        // the producer chose the source before it issued the copy
+        if (ld_shared_u32(sbase + kOffKSrc + 4 * s) == 0u) {  // else: nothing to do
+          const int tj = tile_at(j0, j);
+          const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
+          uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
+          const int rows_valid = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
+          rotate_tile(sbase + kOffK + s * kTileBytes, grow, rows_valid);
+          if (!ok) break;
+          fence_proxy_async_smem();
+          if (share) {
+            // publish this warp's rows of tile tj: each lane's stores, then
+            // one flag per warp (release)
+            fence_proxy_async_global();
+            fence_acq_rel_gpu();
+            __syncwarp();
+            if (lane == 0) {
+              fence_acq_rel_gpu();
+              st_relaxed_gpu_u64(
+                  kflags + ((static_cast<int64_t>(b) * H + h) * n_tiles + tj) * 4 + (u >> 5), token);
+            }
+          }
+          warp_arrive(bar(kBarKFull + s), lane);
+        }
       }
     }
   }
@@ -631,9 +732,28 @@ bool make_table_map(CUtensorMap *map, const uint32_t *table, int64_t S) {
 
 }  // namespace
 
+// A value no earlier launch in this process used, for the exchange flags: a
+// flag equal to it was written during this launch. The counter is mixed
+// (splitmix64 finaliser) with a per-process salt so that stale flag words
+// left in reused memory, by this or another process, match with
+// probability about 2^-64.
+uint64_t next_launch_token() {
+  static std::atomic<uint64_t> counter{0};
+  static const uint64_t salt = [] {
+    std::random_device rd;
+    return (static_cast<uint64_t>(rd()) << 32) ^ rd() ^
+           static_cast<uint64_t>(std::chrono::steady_clock::now().time_since_epoch().count());
+  }();
+  uint64_t z = salt + 0x9E3779B97F4A7C15ull * (counter.fetch_add(1) + 1);
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  z ^= z >> 31;
+  return z == 0 ? 1 : z;
+}
+
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
-                                   cudaStream_t stream) {
+                                   void *krot_scratch, cudaStream_t stream) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -650,6 +770,16 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
       !make_head_map(&maps.v, v, B, S, H) || !make_table_map(&maps.table, table, S))
     return cudaErrorInvalidValue;
+  uint64_t *kflags = nullptr;
+  uint16_t *krot = nullptr;
+  if (krot_scratch != nullptr) {
+    kflags = static_cast<uint64_t *>(krot_scratch);
+    krot = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(krot_scratch) +
+                                        krot_flag_bytes(B, S, H));
+    if (!make_head_map(&maps.krot, krot, B, S, H)) return cudaErrorInvalidValue;
+  } else {
+    maps.krot = maps.k;  // never read
+  }
   // persistent: one CTA per SM, work items handed out round robin
   static int sm_count[64];
   if (sm_count[dev] == 0) {
@@ -662,7 +792,8 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
   joint_rope_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items));
+      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items), kflags, krot,
+      next_launch_token());
   return cudaGetLastError();
 }
 

@@ -110,6 +110,24 @@ int flux_rope_tables_packed(const int32_t *ids, int64_t S, const int32_t *axes_d
 size_t flux_joint_rope_attention_workspace(int64_t S, int D);
 
 /*
+ * flux_joint_rope_attention_krot_bytes: bytes of the optional rotated-K
+ * exchange buffer for [B, S, H, D] inputs (D == 128): one 8-byte flag per
+ * (batch, head, 128-key tile, RoPE warp) padded to 256 bytes, then a bf16
+ * [B, S, H, D] copy of K after RoPE. With it the thread blocks that work on
+ * one head at the same time rotate different K tiles, publish them there and
+ * load the tiles others published instead of rotating every tile themselves;
+ * the result is bit-identical either way. Contents need no initialisation
+ * and are meaningless after a call. Returns 0 for shapes the attention
+ * rejects.
+ *
+ * flux_joint_rope_attention_workspace_shared: flux_joint_rope_attention_workspace
+ * (S, D) + flux_joint_rope_attention_krot_bytes(B, S, H, D); a workspace at
+ * least this large makes flux_joint_rope_attention use the exchange buffer.
+ */
+size_t flux_joint_rope_attention_krot_bytes(int B, int64_t S, int H, int D);
+size_t flux_joint_rope_attention_workspace_shared(int B, int64_t S, int H, int D);
+
+/*
  * flux_joint_rope_attention: out = softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v
  * over the joint token sequence [txt ; img], non-causal, per batch element
  * and head.
@@ -126,8 +144,11 @@ size_t flux_joint_rope_attention_workspace(int64_t S, int D);
  *   out        device, bf16 [B, S, H, D], 16-byte aligned, must not overlap q/k/v.
  *   workspace  device, >= flux_joint_rope_attention_workspace(S, D) bytes,
  *              256-byte aligned, owned by the caller and not shared by calls
- *              in flight at the same time. Its status word is cleared by each
- *              call before the attention kernel runs.
+ *              in flight at the same time; must not overlap q, k, v or out
+ *              (FLUX_ERR_ALIAS). Its status word is cleared by each call
+ *              before the attention kernel runs. With at least
+ *              flux_joint_rope_attention_workspace_shared(B, S, H, D) bytes
+ *              its tail serves as the rotated-K exchange buffer.
  *   stream     cudaStream_t as void*.
  *
  * Numerics: bf16 inputs; the RoPE table is built in fp64/fp32 and stored as
@@ -156,12 +177,19 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
  *   status        device int32 word; the kernel writes FLUX_ERR_DEVICE_TIMEOUT
  *                 there if a bounded wait runs out and never writes it
  *                 otherwise (the caller clears it).
+ *   krot_scratch  device, NULL or >= flux_joint_rope_attention_krot_bytes(B, S,
+ *                 H, D) bytes (krot_bytes), 256-byte aligned, not overlapping
+ *                 q, k, v or out, not shared by calls in flight at the same
+ *                 time: the rotated-K exchange buffer. NULL: every thread
+ *                 block rotates every K tile it loads.
  *   stream        cudaStream_t as void*.
- * Returns FLUX_OK when the kernel was enqueued, else a negative status.
+ * Returns FLUX_OK when the kernel was enqueued, else a negative status
+ * (FLUX_ERR_WORKSPACE for a misaligned or short krot_scratch).
  */
 int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
                                      const uint32_t *table, int B, int64_t S, int H, int D,
-                                     void *out, int32_t *status, void *stream);
+                                     void *out, int32_t *status, void *krot_scratch,
+                                     size_t krot_bytes, void *stream);
 
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)

@@ -48,6 +48,20 @@ def test_workspace_size(lib):
     assert lib.flux_joint_rope_attention_workspace(10, 7) == 0
 
 
+def test_krot_and_shared_workspace_sizes(lib):
+    # flags: B*H*ceil(S/128)*4 words of 8 bytes, padded to 256; then bf16 [B, S, H, 128]
+    assert lib.flux_joint_rope_attention_krot_bytes(1, 4608, 32, 128) == 36864 + 4608 * 32 * 256
+    assert lib.flux_joint_rope_attention_krot_bytes(1, 80, 2, 128) == 256 + 80 * 2 * 256
+    # 2 * 3 * 2 tiles * 4 words * 8 B = 384 -> 512
+    assert lib.flux_joint_rope_attention_krot_bytes(2, 129, 3, 128) == 512 + 2 * 129 * 3 * 256
+    assert (lib.flux_joint_rope_attention_workspace_shared(1, 4608, 32, 128)
+            == lib.flux_joint_rope_attention_workspace(4608, 128)
+            + lib.flux_joint_rope_attention_krot_bytes(1, 4608, 32, 128))
+    for B, S, H, D in ((0, 80, 2, 128), (1, 0, 2, 128), (1, 80, 0, 128), (1, 80, 2, 64)):
+        assert lib.flux_joint_rope_attention_krot_bytes(B, S, H, D) == 0
+        assert lib.flux_joint_rope_attention_workspace_shared(B, S, H, D) == 0
+
+
 def _call(lib, **kw):
     args = dict(q=16, k=16 * 1024, v=32 * 1024, txt=None, S_txt=16, img=None, S_img=64, B=1, H=2,
                 D=128, axes=(32, 32, 32, 32), theta=2000.0, out=48 * 1024 * 1024, ws=256 * 4096,
@@ -84,6 +98,8 @@ def _call(lib, **kw):
     (dict(ws=None), -5),
     (dict(ws=256 * 4096 + 16), -5),
     (dict(ws_bytes=100), -5),
+    (dict(ws=256), -9),               # workspace overlaps q
+    (dict(ws=48 * 1024 * 1024), -9),  # workspace overlaps out
 ])
 def test_bad_arguments_rejected_on_host(lib, kw, code):
     assert _call(lib, **kw) == code
@@ -99,3 +115,18 @@ def test_rope_tables_bad_arguments(lib):
     assert lib.flux_rope_tables_packed(None, 4, axes, 4, 2000.0, P(16), None) == -1
     assert lib.flux_rope_tables_packed(P(16), 0, axes, 4, 2000.0, P(16), None) == -2
     assert lib.flux_rope_tables_packed(P(16), 4, bad, 2, 2000.0, P(16), None) == -3
+
+
+def _tabled(lib, krot, krot_bytes, out=48 * 1024 * 1024):
+    P = ctypes.c_void_p
+    return lib.flux_joint_rope_attention_tabled(P(16), P(16 * 1024), P(32 * 1024), P(4096 * 256),
+                                                1, 80, 2, 128, P(out), P(64), None if krot is None
+                                                else P(krot), krot_bytes, None)
+
+
+def test_tabled_exchange_buffer_checked_on_host(lib):
+    need = lib.flux_joint_rope_attention_krot_bytes(1, 80, 2, 128)
+    assert _tabled(lib, 256 * 8192 + 16, need) == -5      # not 256-byte aligned
+    assert _tabled(lib, 256 * 8192, need - 1) == -5        # too small
+    assert _tabled(lib, 256, need) == -9                   # overlaps q
+    assert _tabled(lib, 48 * 1024 * 1024 + 256, need) == -9  # overlaps out

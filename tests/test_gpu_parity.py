@@ -99,6 +99,33 @@ def test_tabled_entry_matches_one_call_entry():
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("B,H,S", [(1, 2, 80), (2, 3, 1000), (1, 4, 4608), (1, 32, 4608)])
+def test_shared_k_rotation_is_bit_identical(B, H, S):
+    """K tiles rotated by another thread block and loaded from the exchange
+    buffer equal the ones a block rotates itself: the output is the same with
+    and without the buffer, whatever the buffer held before (garbage, or the
+    flags and tiles of an earlier launch)."""
+    q = W.normal_bf16((B, S, H, 128), 71 + S).cuda()
+    k = W.normal_bf16((B, S, H, 128), 72 + S).cuda()
+    v = W.normal_bf16((B, S, H, 128), 73 + S).cuda()
+    ids = _dev(W.random_ids(S, 74 + S, 0, 300))
+    table = binding.rope_tables_packed(ids)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ref = binding.joint_rope_attention_tabled(q, k, v, table, status, krot=False)
+    krot = torch.randint(0, 256, (binding.krot_bytes(B, S, H),), dtype=torch.uint8,
+                         device="cuda")
+    a = binding.joint_rope_attention_tabled(q, k, v, table, status, krot=krot)
+    b = binding.joint_rope_attention_tabled(q, k, v, table, status, krot=krot)
+    # a different K through the same buffer: its stale flags must not be trusted
+    k2 = W.normal_bf16((B, S, H, 128), 75 + S).cuda()
+    ref2 = binding.joint_rope_attention_tabled(q, k2, v, table, status, krot=False)
+    c = binding.joint_rope_attention_tabled(q, k2, v, table, status, krot=krot)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(a, ref) and torch.equal(b, ref)
+    assert torch.equal(c, ref2)
+
+
 def test_rope_tables_zero_ids_are_identity():
     c, s = binding.rope_tables(torch.zeros((300, 4), dtype=torch.int32, device="cuda"))
     torch.cuda.synchronize()
@@ -227,6 +254,9 @@ def test_full_workload_sampled_rows(name):
     out = _run_gpu(q, k, v, txt, img)
     rows = _sample_rows(w.S, w.S_txt, 24, seed=w.index)
     _compare(out, q, k, v, txt, img, rows=rows)
+    # the smallest workspace (no rotated-K exchange) gives the same bits
+    ws = torch.zeros(binding.workspace_bytes(w.S), dtype=torch.uint8, device="cuda")
+    assert torch.equal(_run_gpu(q, k, v, txt, img, workspace=ws), out)
     # every output finite and bounded by the largest |v| (a convex combination)
     assert torch.isfinite(out).all()
     assert out.abs().max().item() <= v.abs().max().item() + 1e-2
