@@ -10,19 +10,28 @@
 //
 // Persistent: one CTA per SM walks work items (batch, head, 256-row block)
 // round robin; for each it owns 256 query rows (two 128-row tiles Q0, Q1)
-// and walks every 128-key tile. The K/V rings, the table ring and every
-// barrier phase run on across items, so the next item's Q is loaded and
-// rotated while the current item's last tiles and epilogue finish.
+// and walks every 128-key tile, starting at a tile that depends on its row
+// block (spread evenly over the head). The K/V rings, the table ring and
+// every barrier phase run on across items, so the next item's Q is loaded
+// and rotated while the current item's last tiles and epilogue finish.
 // 16 warps in four warpgroups:
-//   WG0  warp 0: TMA producer of raw Q (once), raw K tiles (2-stage ring) and
+//   WG0  warp 0: TMA producer of raw Q (once), K tiles (2-stage ring) and
 //        the packed (cos, sin) table in 64-token halves (2-buffer ring);
-//        warp 1: MMA issuer (one thread); warp 2: TMEM allocation;
+//        warp 1: MMA issuer (the whole warp walks the schedule, elect.sync
+//        picks the issuing lane); warp 2: TMEM allocation;
 //        warp 3: TMA producer of V tiles (2-stage ring).
 //   WG1  softmax of Q0: thread = TMEM lane = query row.
 //   WG2  softmax of Q1.
 //   WG3  RoPE: rotates each landed Q / K tile in place in shared memory,
 //        one adjacent channel pair per 32-bit word, with the table half
 //        that landed beside it, then hands the tile to the MMA.
+// Rotated K is shared between the CTAs that work on one head: a CTA that
+// rotates a K tile also stores it to an exchange buffer (a bf16 copy of K's
+// layout) and sets one flag per RoPE warp; a CTA whose producer finds all
+// four flags set for this launch loads the rotated tile from there straight
+// into the K stage (no table, no RoPE warps). Staggered start tiles make
+// the CTAs of a head rotate different tiles first. Without the buffer every
+// CTA rotates every K tile it loads; the results are bit-identical.
 // Every global-to-shared copy is a TMA tile copy (128-byte swizzle for Q, K,
 // V; out-of-range tokens read as zeros); nothing on the path waits on a
 // plain global load.
@@ -30,7 +39,7 @@
 // softmax writes P_t as packed bf16 over the first 64 columns of S_t and the
 // MMA reads it from there (A operand in TMEM).
 //
-// Issue order of the MMA thread per key tile j:
+// Issue order of the MMA warp per key tile j:
 //   S0(0) S1(0) | PV0(j) S0(j+1) PV1(j) S1(j+1) | ...
 // tcgen05 MMAs of one thread execute in order, so S_t(j+1) overwrites P_t(j)
 // only after PV_t(j) has read it, and the commit that signals S_t(j+1) also
@@ -38,7 +47,8 @@
 //
 // Softmax runs in the log2 domain with a lazily updated running max: O and l
 // are rescaled only when a row's max grows by more than 8 (a factor 256),
-// which keeps exp2 arguments <= 8 and is exact after the final 1/l.
+// which keeps exp2 arguments <= 8 and is exact after the final 1/l. The row
+// max of a full key tile comes from the TMEM loads' own max reduction.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -102,9 +112,10 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
-constexpr uint32_t kRegsSoftmax = 160;
-constexpr uint32_t kRegsOther = 96;
-static_assert(128 * (2 * kRegsSoftmax + 2 * kRegsOther) == 512 * 128,
+constexpr uint32_t kRegsSoftmax = 176;
+constexpr uint32_t kRegsCopyMma = 88;  // WG0: producers, MMA issuer
+constexpr uint32_t kRegsRope = 72;
+static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
 __device__ __forceinline__ uint32_t sw128_offset(int r, int c16) {
@@ -125,6 +136,9 @@ __device__ __forceinline__ uint32_t rope_pair(uint32_t w, uint32_t cs) {
   const float c = f16lo_to_f32(cs), s = f16hi_to_f32(cs);
   return pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
 }
+
+// Hides a value's origin from the optimiser (no code is emitted).
+__device__ __forceinline__ void opaque(uint64_t &x) { asm volatile("" : "+l"(x)); }
 
 template <uint32_t kRegs>
 __device__ __forceinline__ void reg_inc() {
@@ -148,24 +162,28 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
                                             int rows_valid = 0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
-  uint4 w[8], cs[8];
+  // two batches of four rows: all loads of a batch in flight together
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rh = i * 8 + rsub;
-    w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
-    cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
-  }
+  for (int i0 = 0; i0 < 8; i0 += 4) {
+    uint4 w[4], cs[4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int rh = i * 8 + rsub;
-    uint4 o;
-    o.x = rope_pair(w[i].x, cs[i].x);
-    o.y = rope_pair(w[i].y, cs[i].y);
-    o.z = rope_pair(w[i].z, cs[i].z);
-    o.w = rope_pair(w[i].w, cs[i].w);
-    st_shared_v4(tile + sw128_offset(half * 64 + rh, c16), o);
-    if (kPublish && half * 64 + rh < rows_valid)
-      st_global_v4(grow + (half * 64 + rh) * row_stride + c16 * 8, o);
+    for (int i = 0; i < 4; ++i) {
+      const int rh = (i0 + i) * 8 + rsub;
+      w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
+      cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rh = (i0 + i) * 8 + rsub;
+      uint4 o;
+      o.x = rope_pair(w[i].x, cs[i].x);
+      o.y = rope_pair(w[i].y, cs[i].y);
+      o.z = rope_pair(w[i].z, cs[i].z);
+      o.w = rope_pair(w[i].w, cs[i].w);
+      st_shared_v4(tile + sw128_offset(half * 64 + rh, c16), o);
+      if (kPublish && half * 64 + rh < rows_valid)
+        st_global_v4(grow + (half * 64 + rh) * row_stride + c16 * 8, o);
+    }
   }
 }
 
@@ -277,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
 
   if (warp < 4) {
-    reg_dec<kRegsOther>();
+    reg_dec<kRegsCopyMma>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------- producer: Q, K (raw) and table
       tma_prefetch_desc(&maps.q);
@@ -410,8 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk0 = desc_kmajor(sbase + kOffK, 0);
       const uint64_t dv0 = desc_v(sbase + kOffV, 0);
       auto issue_s = [&](int t, int sk) {
-        const uint64_t da = desc_advance(dq0, t * kTileBytes);
-        const uint64_t db = desc_advance(dk0, sk * kTileBytes);
+        uint64_t da = desc_advance(dq0, t * kTileBytes);
+        uint64_t db = desc_advance(dk0, sk * kTileBytes);
+        opaque(da);  // per-MMA descriptors are base + constant, computed here,
+        opaque(db);  // not hoisted into registers for every (t, stage, kk)
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
@@ -438,7 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < n_tiles; ++j) {
           const int g0 = jt + j;  // global tile of this step
           const int sv = g0 % kStages;
-          const uint64_t dv = desc_advance(dv0, sv * kTileBytes);
+          uint64_t dv = desc_advance(dv0, sv * kTileBytes);
+          opaque(dv);
           const bool more = j + 1 < n_tiles;
           const int sk = (g0 + 1) % kStages;
           if (!(ok = mbar_wait_warp(bar(kBarVFull + sv), static_cast<uint32_t>(g0 / kStages) & 1u,
@@ -504,26 +525,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
         tc_fence_after_sync();
         uint32_t sr[kBN];
+        float mr[kBN / 32];
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c)
-          tmem_ld32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+          tmem_ld32_max(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]), mr[c]);
         tmem_ld_wait();
         const int valid = static_cast<int>(S - static_cast<int64_t>(tile_at(j0, j)) * kBN);
+        float mx = fmax3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
         if (valid < kBN) {
 #pragma unroll
           for (int i = 0; i < kBN; ++i)
             if (i >= valid) sr[i] = __float_as_uint(-INFINITY);
-        }
-        // row max: four independent chains of 3-input max
-        float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
+          // row max: four independent chains of 3-input max
+          float ma = -INFINITY, mb = -INFINITY, mc = -INFINITY, md = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < kBN; i += 8) {
-          ma = fmax3(ma, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
-          mb = fmax3(mb, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
-          mc = fmax3(mc, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
-          md = fmax3(md, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+          for (int i = 0; i < kBN; i += 8) {
+            ma = fmax3(ma, __uint_as_float(sr[i]), __uint_as_float(sr[i + 1]));
+            mb = fmax3(mb, __uint_as_float(sr[i + 2]), __uint_as_float(sr[i + 3]));
+            mc = fmax3(mc, __uint_as_float(sr[i + 4]), __uint_as_float(sr[i + 5]));
+            md = fmax3(md, __uint_as_float(sr[i + 6]), __uint_as_float(sr[i + 7]));
+          }
+          mx = fmax3(ma, mb, fmaxf(mc, md));
         }
-        float mx = fmax3(ma, mb, fmaxf(mc, md));
         mx *= scale_log2;
         float alpha = 1.f;
         float m_use = m_run;
@@ -608,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- RoPE warps
-    reg_dec<kRegsOther>();
+    reg_dec<kRegsRope>();
     const int u = tid - 384;
     int g = 0;   // table halves consumed so far
     int jt = 0;  // K tiles consumed so far
