@@ -80,6 +80,12 @@ constexpr uint32_t kTableHalfBytes = kHalfRows * kPairs * 4;  // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kQPrefetchTiles = 6;  // key tiles before an item's end its successor's Q is prefetched
+constexpr int kPrepAtTile = 2;      // key tile of an item before which the RoPE warps prepare the next
+// RoPE work queue entry: x = kind | stage << 4 | phase parity << 8 | tile << 9, y = item
+constexpr uint32_t kRqQ = 1;     // rotate the item's two Q tiles in place (Q-raw -> Q-full)
+constexpr uint32_t kRqK = 2;     // rotate a raw K tile in place (K-raw -> K-full), publish it
+constexpr uint32_t kRqPrep = 3;  // prepare item y (rotated Q to the exchange buffer, first K tiles)
+constexpr uint32_t kRqEnd = 4;   // no more work
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;                                   // Q0, Q1
@@ -102,19 +108,23 @@ constexpr int kBarPFull = kBarSFull + kQTiles;
 constexpr int kBarODone = kBarPFull + kQTiles;
 constexpr int kBarOFree = kBarODone + kQTiles;  // epilogue done reading O_t
 constexpr int kBarQFree = kBarOFree + kQTiles;  // every S MMA of an item done
-constexpr int kBarDrain = kBarQFree + 1;
+constexpr int kBarQPrep = kBarQFree + 1;  // next item's rotated Q is in the exchange buffer
+constexpr int kRopeQ = 8;                  // RoPE work queue entries
+constexpr int kBarRQFull = kBarQPrep + 1;  // + entry
+constexpr int kBarRQEmpty = kBarRQFull + kRopeQ;
+constexpr int kBarDrain = kBarRQEmpty + kRopeQ;
 constexpr int kNumBars = kBarDrain + 1;
 constexpr uint32_t kOffTmemSlot = kOffBar + kNumBars * 8;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kOffKSrc = kOffAbort + 4;  // per K stage: 1 = landed already rotated
-constexpr uint32_t kSmemUsed = kOffKSrc + 4 * kStages;
+constexpr uint32_t kOffRQ = (kOffAbort + 4 + 7) & ~7u;  // RoPE work queue: uint2 per entry
+constexpr uint32_t kSmemUsed = kOffRQ + 8 * kRopeQ;
 constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
-constexpr uint32_t kRegsSoftmax = 176;
+constexpr uint32_t kRegsSoftmax = 168;
 constexpr uint32_t kRegsCopyMma = 88;  // WG0: producers, MMA issuer
-constexpr uint32_t kRegsRope = 72;
+constexpr uint32_t kRegsRope = 88;
 static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -187,8 +197,44 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
   }
 }
 
+// 128 RoPE threads rotate `nrows` rows of one head from global memory to
+// global memory: src / dst point at the first row's channel 0, rows are
+// row_stride elements apart, `tab` at the first row's packed table row. Thread
+// u owns 16-byte chunk u & 15 of rows (u >> 4) + 8 i, the row-to-thread map of
+// rotate_half, so RoPE warp w writes the rows r with r mod 8 in {2w, 2w+1}.
+__device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t *dst,
+                                                   const uint32_t *tab, int nrows,
+                                                   int64_t row_stride, int u) {
+  const int c16 = u & 15;
+  const int rsub = u >> 4;
+#pragma unroll 1
+  for (int i0 = 0; rsub + 8 * i0 < nrows; i0 += 2) {
+    uint4 w[2], cs[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = rsub + 8 * (i0 + i);
+      if (r < nrows) {
+        w[i] = ld_global_nc_v4(src + r * row_stride + c16 * 8);
+        cs[i] = ld_global_nc_v4(tab + static_cast<int64_t>(r) * kPairs + c16 * 4);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int r = rsub + 8 * (i0 + i);
+      if (r < nrows) {
+        uint4 o;
+        o.x = rope_pair(w[i].x, cs[i].x);
+        o.y = rope_pair(w[i].y, cs[i].y);
+        o.z = rope_pair(w[i].z, cs[i].z);
+        o.w = rope_pair(w[i].w, cs[i].w);
+        st_global_v4(dst + r * row_stride + c16 * 8, o);
+      }
+    }
+  }
+}
+
 struct Maps {
-  CUtensorMap q, k, v, table, krot;
+  CUtensorMap q, k, v, table, krot, qrot;
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -223,7 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
                                 int *__restrict__ status, int64_t S, int H, int n_items,
                                 uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
-                                uint64_t token) {
+                                uint16_t *__restrict__ qrot, const uint16_t *__restrict__ qg,
+                                const uint16_t *__restrict__ kg,
+                                const uint32_t *__restrict__ tabg, uint64_t token) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -278,6 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarOFree + t), 4);
     }
     mbar_init(bar(kBarQFree), 1);
+    mbar_init(bar(kBarQPrep), 4);
+    for (int e = 0; e < kRopeQ; ++e) {
+      mbar_init(bar(kBarRQFull + e), 1);
+      mbar_init(bar(kBarRQEmpty + e), 4);
+    }
     mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -297,14 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     reg_dec<kRegsCopyMma>();
     if (warp == 0 && lane == 0) {
-      // ------------------------------------- producer: Q, K (raw) and table
+      // ------------------------------------- producer: Q, K and the table
+      // Every copy that needs rotating is announced to the RoPE warps through
+      // the work queue (before its table halves, which the RoPE warps free);
+      // already rotated tiles go straight to the MMA.
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
       tma_prefetch_desc(&maps.table);
-      if (share) tma_prefetch_desc(&maps.krot);
+      if (share) {
+        tma_prefetch_desc(&maps.krot);
+        tma_prefetch_desc(&maps.qrot);
+      }
       int g = 0;   // table halves issued so far
       int jt = 0;  // K tiles issued so far (all items)
-      uint32_t rot_mask = 0;  // bit s: the last copy into K stage s was an already rotated tile
+      int pq = 0;  // queue entries posted so far
       bool ok = true;
       auto table_half = [&](int row0) {
         const int buf = g & 1;
@@ -315,33 +374,79 @@ __global__ void __launch_bounds__(kThreads, 1)
                     row0);
         ++g;
       };
+      auto post = [&](uint32_t x, uint32_t y) {
+        const int e = pq % kRopeQ;
+        const uint32_t use = static_cast<uint32_t>(pq / kRopeQ);
+        if (!(ok = mbar_wait(bar(kBarRQEmpty + e), (use & 1u) ^ 1u, abort_flag))) return;
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(sbase + kOffRQ + 8 * e), "r"(x),
+                     "r"(y)
+                     : "memory");
+        mbar_arrive(bar(kBarRQFull + e));  // release: the entry is visible to the waiters
+        ++pq;
+      };
       int k = 0;
-      int q_loads = 0;
+      int q_local = 0;                 // Q loads rotated in place (Q-raw phases)
+      // bit s: parity of the raw K copies into stage s so far (K-raw phases)
+      uint32_t raw_par = 0;
+      int last_q_bar = -1;  // barrier / parity the last Q copy completes
+      uint32_t last_q_parity = 0;
+      // per K stage s (bit s): the last copy went straight to K-full, and the
+      // parity of the phase it completes
+      uint32_t last_k_full = 0, last_k_par = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
         int b, h, m0;
         decode(item, b, h, m0);
+        const int next = item + static_cast<int>(gridDim.x);
         // the previous item's S MMAs no longer read the Q buffers
         if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
           break;
-        ++q_loads;
-        mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
-        for (int t = 0; t < kQTiles; ++t) {
-          const uint32_t dst = sbase + kOffQ + t * kTileBytes;
-          tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
-          tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
+        if (share && k > 0) {
+          // The RoPE warps rotated this item's Q into the exchange buffer
+          // during the previous item: copy it in rotated, completing Q-full
+          // (its other three arrivals made here) without the RoPE warps.
+          if (!(ok = mbar_wait(bar(kBarQPrep), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
+            break;
+          fence_proxy_async_global();
+          last_q_bar = kBarQFull;
+          last_q_parity = static_cast<uint32_t>(k) & 1u;
+          mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
+          for (int t = 0; t < kQTiles; ++t) {
+            const uint32_t dst = sbase + kOffQ + t * kTileBytes;
+            tma_load_4d(dst, &maps.qrot, bar(kBarQFull), 0, h, m0 + t * kBM, b);
+            tma_load_4d(dst + kBlockBytes, &maps.qrot, bar(kBarQFull), 64, h, m0 + t * kBM, b);
+          }
+          mbar_arrive_n(bar(kBarQFull), 3);
+        } else {
+          last_q_bar = kBarQRaw;
+          last_q_parity = static_cast<uint32_t>(q_local) & 1u;
+          mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
+          for (int t = 0; t < kQTiles; ++t) {
+            const uint32_t dst = sbase + kOffQ + t * kTileBytes;
+            tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
+            tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
+          }
+          post(kRqQ | (last_q_parity << 8), static_cast<uint32_t>(item));
+          ++q_local;
+          for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
         }
-        for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
         const int j0 = first_tile(m0);
+        const int prep_at = n_tiles > kPrepAtTile ? kPrepAtTile : n_tiles - 1;
         const uint64_t *fl_head =
             share ? kflags + (static_cast<int64_t>(b) * H + h) * n_tiles * 4 : nullptr;
         for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
+          if (share && j == prep_at && next < n_items) {
+            post(kRqPrep, static_cast<uint32_t>(next));
+            if (!ok) break;
+          }
           const int s = jt % kStages;
           const int tj = tile_at(j0, j);
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           // Has every RoPE warp of some CTA published tile tj? Decided (and
           // the acquire fence paid) before the ring wait, which hides both.
-          bool rotated = false;
-          if (share) {
+          // The first two tiles of a prepared item were rotated by this CTA's
+          // RoPE warps, ordered before this point by the Q-prep wait.
+          bool rotated = share && k > 0 && j < 2;
+          if (share && !rotated) {
             const uint64_t *fl = fl_head + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
             ld_relaxed_gpu_v2_u64(fl, f0, f1);
@@ -353,30 +458,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
-          st_shared_u32(sbase + kOffKSrc + 4 * s, rotated ? 1u : 0u);
-          rot_mask = rotated ? (rot_mask | (1u << s)) : (rot_mask & ~(1u << s));
           const uint32_t dst = sbase + kOffK + s * kTileBytes;
           if (rotated) {
             // straight to the MMA: the copy completes K-full, whose other
-            // three arrivals are made here; the RoPE warps only see K-raw
-            // complete and skip the tile
-            mbar_arrive(bar(kBarKRaw + s));
+            // three arrivals are made here
+            last_k_full |= 1u << s;
+            last_k_par = (last_k_par & ~(1u << s)) | ((use & 1u) << s);
             mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
             tma_load_4d(dst, &maps.krot, bar(kBarKFull + s), 0, h, tj * kBN, b);
             tma_load_4d(dst + kBlockBytes, &maps.krot, bar(kBarKFull + s), 64, h, tj * kBN, b);
             mbar_arrive_n(bar(kBarKFull + s), 3);
           } else {
+            const uint32_t par = (raw_par >> s) & 1u;
+            raw_par ^= 1u << s;
+            last_k_full &= ~(1u << s);
+            last_k_par = (last_k_par & ~(1u << s)) | (par << s);
             mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
             tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, tj * kBN, b);
             tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, tj * kBN, b);
-            table_half(tj * kBN);
+            post(kRqK | (static_cast<uint32_t>(s) << 4) | (par << 8) |
+                     (static_cast<uint32_t>(tj) << 9),
+                 static_cast<uint32_t>(item));
+            if (ok) table_half(tj * kBN);
             if (ok) table_half(tj * kBN + static_cast<int>(kHalfRows));
           }
-          // the next item's Q into L2 a few tiles before it is loaded
-          if (j == (n_tiles > kQPrefetchTiles ? n_tiles - kQPrefetchTiles : 0) &&
-              item + static_cast<int>(gridDim.x) < n_items) {
+          // the next item's raw Q into L2 a few tiles before it is loaded (with
+          // the exchange buffer the RoPE warps have read it long before)
+          if (!share && j == (n_tiles > kQPrefetchTiles ? n_tiles - kQPrefetchTiles : 0) &&
+              next < n_items) {
             int nb, nh, nm0;
-            decode(item + static_cast<int>(gridDim.x), nb, nh, nm0);
+            decode(next, nb, nh, nm0);
             for (int t = 0; t < kQTiles && nm0 + t * kBM < S; ++t) {
               tma_prefetch_l2_4d(&maps.q, 0, nh, nm0 + t * kBM, nb);
               tma_prefetch_l2_4d(&maps.q, 64, nh, nm0 + t * kBM, nb);
@@ -384,13 +495,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      if (ok) post(kRqEnd, 0);
       {  // every copy issued above has landed before the CTA exits (a no-op
          // unless an abort left some unconsumed)
-        if (q_loads > 0) drain_wait(bar(kBarQRaw), static_cast<uint32_t>(q_loads - 1) & 1u);
+        if (last_q_bar >= 0) drain_wait(bar(last_q_bar), last_q_parity);
         for (int jj = (jt > kStages ? jt - kStages : 0); jj < jt; ++jj) {
-          const int sj = jj % kStages;  // a rotated tile's copy completes K-full
-          drain_wait(bar(((rot_mask >> sj) & 1u) ? kBarKFull + sj : kBarKRaw + sj),
-                     static_cast<uint32_t>(jj / kStages) & 1u);
+          const int sj = jj % kStages;
+          drain_wait(bar(((last_k_full >> sj) & 1u) ? kBarKFull + sj : kBarKRaw + sj),
+                     (last_k_par >> sj) & 1u);
         }
         for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
           drain_wait(bar(kBarTFull + (gg & 1)), static_cast<uint32_t>(gg >> 1) & 1u);
@@ -633,8 +745,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- RoPE warps
     reg_dec<kRegsRope>();
     const int u = tid - 384;
-    int g = 0;   // table halves consumed so far
-    int jt = 0;  // K tiles consumed so far
+    int g = 0;  // table halves consumed so far
     bool ok = true;
     // Rotates a landed tile in place; with `grow` (K tiles when sharing) the
     // rotated rows also go to the exchange buffer.
@@ -652,45 +763,108 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++g;
       }
     };
-    int k = 0;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
-      if (!(ok = mbar_wait_warp(bar(kBarQRaw), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
-      for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes, nullptr, 0);
-      if (!ok) break;
-      fence_proxy_async_smem();
-      warp_arrive(bar(kBarQFull), lane);
-      int b, h, m0;
-      decode(item, b, h, m0);
-      const int j0 = first_tile(m0);
-      for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
-        const int s = jt % kStages;
-        if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), static_cast<uint32_t>(jt / kStages) & 1u,
-                             abort_flag)))
-          break;
-        // the producer chose the source before it issued the copy
-        if (ld_shared_u32(sbase + kOffKSrc + 4 * s) == 0u) {  // else: nothing to do
-          const int tj = tile_at(j0, j);
-          const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
-          uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
-          const int rows_valid = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
-          rotate_tile(sbase + kOffK + s * kTileBytes, grow, rows_valid);
-          if (!ok) break;
-          fence_proxy_async_smem();
-          if (share) {
-            // publish this warp's rows of tile tj: each lane's stores, then
-            // one flag per warp (release)
-            fence_proxy_async_global();
+    // Prepares the CTA's next item while the current one runs: its Q rows and
+    // its first two K tiles rotated into the exchange buffer (the K tiles
+    // also published for other CTAs: a tile someone already published is
+    // rewritten with the same bytes), then Q-prep, after which the producer
+    // loads all three without reading flags.
+    auto prepare_next = [&](int next) {
+      int nb, nh, nm0;
+      decode(next, nb, nh, nm0);
+      const int nj0 = first_tile(nm0);
+      // job 0: the Q rows; jobs 1, 2: the first two K tiles (one call site
+      // of the rotation keeps the RoPE warps' register budget)
+#pragma unroll 1
+      for (int job = 0; job < 3; ++job) {
+        int64_t tok0;
+        int nrows;
+        const uint16_t *src;
+        uint16_t *dst;
+        uint64_t *fl = nullptr;
+        if (job == 0) {
+          tok0 = nm0;
+          nrows = static_cast<int>(S - tok0 < kRowsPerCta ? S - tok0 : kRowsPerCta);
+          const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
+          src = qg + o;
+          dst = qrot + o;
+        } else {
+          if (job - 1 >= n_tiles) break;
+          const int tj = tile_at(nj0, job - 1);
+          fl = kflags + ((static_cast<int64_t>(nb) * H + nh) * n_tiles + tj) * 4;
+          tok0 = static_cast<int64_t>(tj) * kBN;
+          nrows = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
+          const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
+          src = kg + o;
+          dst = krot + o;
+        }
+        rotate_rows_global(src, dst, tabg + tok0 * kPairs, nrows, row_stride, u);
+        fence_proxy_async_global();  // read by TMA copies
+        if (job > 0) {
+          // publish as the in-place path does: this warp's rows, then its flag
+          fence_acq_rel_gpu();
+          __syncwarp();
+          if (lane == 0) {
             fence_acq_rel_gpu();
-            __syncwarp();
-            if (lane == 0) {
-              fence_acq_rel_gpu();
-              st_relaxed_gpu_u64(
-                  kflags + ((static_cast<int64_t>(b) * H + h) * n_tiles + tj) * 4 + (u >> 5), token);
-            }
+            st_relaxed_gpu_u64(fl + (u >> 5), token);
           }
-          warp_arrive(bar(kBarKFull + s), lane);
         }
       }
+      warp_arrive(bar(kBarQPrep), lane);
+    };
+    // Work comes from the producer's queue in issue order; every rotation
+    // step, the table ring and each wait are this warp's alone (one arrival
+    // per warp on the hand-off barriers), so the warps never wait on each
+    // other.
+    for (int qi = 0; ok; ++qi) {
+      const int e = qi % kRopeQ;
+      if (!(ok = mbar_wait_warp(bar(kBarRQFull + e), static_cast<uint32_t>(qi / kRopeQ) & 1u,
+                                abort_flag)))
+        break;
+      uint32_t x, y;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(x), "=r"(y) : "r"(sbase + kOffRQ + 8 * e)
+                   : "memory");
+      warp_arrive(bar(kBarRQEmpty + e), lane);  // the slot may be reused
+      const uint32_t kind = x & 15u;
+      if (kind == kRqEnd) break;
+      const int item = static_cast<int>(y);
+      if (kind == kRqPrep) {
+        prepare_next(item);
+        continue;
+      }
+      const uint32_t par = (x >> 8) & 1u;
+      if (kind == kRqQ) {
+        if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
+        for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes, nullptr, 0);
+        if (!ok) break;
+        fence_proxy_async_smem();
+        warp_arrive(bar(kBarQFull), lane);
+        continue;
+      }
+      // kind == kRqK: a raw K tile in stage s
+      const int s = static_cast<int>((x >> 4) & 15u);
+      const int tj = static_cast<int>(x >> 9);
+      int b, h, m0;
+      decode(item, b, h, m0);
+      if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
+      const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
+      uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
+      const int rows_valid = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
+      rotate_tile(sbase + kOffK + s * kTileBytes, grow, rows_valid);
+      if (!ok) break;
+      fence_proxy_async_smem();
+      if (share) {
+        // publish this warp's rows of tile tj: each lane's stores, then
+        // one flag per warp (release)
+        fence_proxy_async_global();
+        fence_acq_rel_gpu();
+        __syncwarp();
+        if (lane == 0) {
+          fence_acq_rel_gpu();
+          st_relaxed_gpu_u64(
+              kflags + ((static_cast<int64_t>(b) * H + h) * n_tiles + tj) * 4 + (u >> 5), token);
+        }
+      }
+      warp_arrive(bar(kBarKFull + s), lane);
     }
   }
 
@@ -794,14 +968,18 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
       !make_head_map(&maps.v, v, B, S, H) || !make_table_map(&maps.table, table, S))
     return cudaErrorInvalidValue;
   uint64_t *kflags = nullptr;
-  uint16_t *krot = nullptr;
+  uint16_t *krot = nullptr, *qrot = nullptr;
   if (krot_scratch != nullptr) {
+    const size_t tensor = static_cast<size_t>(B) * static_cast<size_t>(S) * H * kD * 2;
     kflags = static_cast<uint64_t *>(krot_scratch);
     krot = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(krot_scratch) +
                                         krot_flag_bytes(B, S, H));
-    if (!make_head_map(&maps.krot, krot, B, S, H)) return cudaErrorInvalidValue;
+    qrot = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(krot) + tensor);
+    if (!make_head_map(&maps.krot, krot, B, S, H) || !make_head_map(&maps.qrot, qrot, B, S, H))
+      return cudaErrorInvalidValue;
   } else {
     maps.krot = maps.k;  // never read
+    maps.qrot = maps.q;
   }
   // persistent: one CTA per SM, work items handed out round robin
   static int sm_count[64];
@@ -815,7 +993,8 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
   joint_rope_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items), kflags, krot,
+      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items), kflags, krot, qrot,
+      static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k), table,
       next_launch_token());
   return cudaGetLastError();
 }

@@ -47,10 +47,10 @@ inline size_t packed_table_bytes(int64_t S, int D) {
   return (b + 255) & ~static_cast<size_t>(255);
 }
 
-// Rotated-K exchange buffer of the attention kernel for [B, S, H, D] inputs:
-// one 8-byte flag per (batch, head, key tile, RoPE warp), padded to 256 bytes,
-// then a [B, S, H, D] bf16 copy of K after RoPE. 0 if D is not 128 or the
-// size overflows.
+// Exchange buffer of the attention kernel for [B, S, H, D] inputs: one 8-byte
+// flag per (batch, head, key tile, RoPE warp), padded to 256 bytes, then a
+// [B, S, H, D] bf16 copy of K after RoPE, then one of Q after RoPE. 0 if D is
+// not 128 or the shape is empty.
 inline size_t krot_flag_bytes(int B, int64_t S, int H) {
   const size_t tiles = static_cast<size_t>((S + 127) / 128);
   size_t b = static_cast<size_t>(B) * static_cast<size_t>(H) * tiles * 4 * sizeof(uint64_t);
@@ -59,7 +59,7 @@ inline size_t krot_flag_bytes(int B, int64_t S, int H) {
 inline size_t krot_scratch_bytes(int B, int64_t S, int H, int D) {
   if (D != 128 || B < 1 || H < 1 || S < 1) return 0;
   return krot_flag_bytes(B, S, H) +
-         static_cast<size_t>(B) * static_cast<size_t>(S) * static_cast<size_t>(H) * 128 * 2;
+         2 * static_cast<size_t>(B) * static_cast<size_t>(S) * static_cast<size_t>(H) * 128 * 2;
 }
 
 // Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`

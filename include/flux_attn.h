@@ -110,15 +110,15 @@ int flux_rope_tables_packed(const int32_t *ids, int64_t S, const int32_t *axes_d
 size_t flux_joint_rope_attention_workspace(int64_t S, int D);
 
 /*
- * flux_joint_rope_attention_krot_bytes: bytes of the optional rotated-K
- * exchange buffer for [B, S, H, D] inputs (D == 128): one 8-byte flag per
- * (batch, head, 128-key tile, RoPE warp) padded to 256 bytes, then a bf16
- * [B, S, H, D] copy of K after RoPE. With it the thread blocks that work on
- * one head at the same time rotate different K tiles, publish them there and
- * load the tiles others published instead of rotating every tile themselves;
- * the result is bit-identical either way. Contents need no initialisation
- * and are meaningless after a call. Returns 0 for shapes the attention
- * rejects.
+ * flux_joint_rope_attention_krot_bytes: bytes of the optional exchange
+ * buffer for [B, S, H, D] inputs (D == 128): one 8-byte flag per (batch,
+ * head, 128-key tile, RoPE warp) padded to 256 bytes, then bf16 [B, S, H, D]
+ * copies of K and of Q after RoPE. With it the thread blocks that work on one
+ * head at the same time rotate different K tiles, publish them there and load
+ * the tiles others published instead of rotating every tile themselves, and
+ * each block rotates its next work item's Q rows ahead of time; the result is
+ * bit-identical either way. Contents need no initialisation and are
+ * meaningless after a call. Returns 0 for shapes the attention rejects.
  *
  * flux_joint_rope_attention_workspace_shared: flux_joint_rope_attention_workspace
  * (S, D) + flux_joint_rope_attention_krot_bytes(B, S, H, D); a workspace at

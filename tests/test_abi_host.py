@@ -49,11 +49,14 @@ def test_workspace_size(lib):
 
 
 def test_krot_and_shared_workspace_sizes(lib):
-    # flags: B*H*ceil(S/128)*4 words of 8 bytes, padded to 256; then bf16 [B, S, H, 128]
-    assert lib.flux_joint_rope_attention_krot_bytes(1, 4608, 32, 128) == 36864 + 4608 * 32 * 256
-    assert lib.flux_joint_rope_attention_krot_bytes(1, 80, 2, 128) == 256 + 80 * 2 * 256
+    # flags: B*H*ceil(S/128)*4 words of 8 bytes, padded to 256; then rotated K
+    # and rotated Q, each bf16 [B, S, H, 128]
+    assert (lib.flux_joint_rope_attention_krot_bytes(1, 4608, 32, 128)
+            == 36864 + 2 * 4608 * 32 * 256)
+    assert lib.flux_joint_rope_attention_krot_bytes(1, 80, 2, 128) == 256 + 2 * 80 * 2 * 256
     # 2 * 3 * 2 tiles * 4 words * 8 B = 384 -> 512
-    assert lib.flux_joint_rope_attention_krot_bytes(2, 129, 3, 128) == 512 + 2 * 129 * 3 * 256
+    assert (lib.flux_joint_rope_attention_krot_bytes(2, 129, 3, 128)
+            == 512 + 2 * 2 * 129 * 3 * 256)
     assert (lib.flux_joint_rope_attention_workspace_shared(1, 4608, 32, 128)
             == lib.flux_joint_rope_attention_workspace(4608, 128)
             + lib.flux_joint_rope_attention_krot_bytes(1, 4608, 32, 128))

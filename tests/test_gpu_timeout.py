@@ -1,8 +1,8 @@
 """Failure detection without a GPU fault: a bounded wait that runs out.
 
 The test compiles a copy of the library in which the RoPE warps of every
-CTA withhold their hand-off of the first K tile (a barrier arrival that
-nothing else provides). The MMA thread's wait on it is bounded (about a
+CTA withhold their hand-off of key tile 0 (a barrier arrival that nothing
+else provides; without the exchange buffer every K tile goes through them). The MMA thread's wait on it is bounded (about a
 second of clock cycles); when it runs out the kernel raises its abort flag,
 every other role leaves its loop, copies still in flight are waited for,
 TMEM is released and FLUX_ERR_DEVICE_TIMEOUT lands in the status word. No
@@ -26,7 +26,7 @@ from diffusion_transformer_joint_gb300 import workloads as W
 pytestmark = pytest.mark.gpu
 
 ANCHOR = "warp_arrive(bar(kBarKFull + s), lane);"
-WITHHELD = "if (jt != 0) warp_arrive(bar(kBarKFull + s), lane);"
+WITHHELD = "if (tj != 0) warp_arrive(bar(kBarKFull + s), lane);"
 
 
 def _build_withholding_library(tmp_path):
