@@ -75,24 +75,24 @@ constexpr int kStages = 2;  // K and V ring depth
 constexpr int kPairs = kD / 2;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;
 constexpr uint32_t kBlockBytes = 16384;          // one 64-channel swizzle block
-constexpr uint32_t kHalfRows = 64;               // table rows per table buffer
-constexpr uint32_t kTableHalfBytes = kHalfRows * kPairs * 4;  // 16 KB
+constexpr uint32_t kStageWarpBytes = 32 * 128;  // epilogue staging: 32 rows x 64 channels bf16
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kQPrefetchTiles = 6;  // key tiles before an item's end its successor's Q is prefetched
-constexpr int kPrepAtTile = 2;      // key tile of an item before which the RoPE warps prepare the next
+constexpr int kPrepAtTile = 2;      // key tile of an item from which the next one is prepared
+constexpr int kPrepChunks = 8;      // 64-row pieces: 4 of Q, 2 per K tile for the first two K tiles
 // RoPE work queue entry: x = kind | stage << 4 | phase parity << 8 | tile << 9, y = item
 constexpr uint32_t kRqQ = 1;     // rotate the item's two Q tiles in place (Q-raw -> Q-full)
 constexpr uint32_t kRqK = 2;     // rotate a raw K tile in place (K-raw -> K-full), publish it
-constexpr uint32_t kRqPrep = 3;  // prepare item y (rotated Q to the exchange buffer, first K tiles)
+constexpr uint32_t kRqPrep = 3;  // prepare piece (x >> 4) of item y (rotated Q / first K tiles)
 constexpr uint32_t kRqEnd = 4;   // no more work
 
 // Shared-memory map (offsets from a 1024-byte aligned base).
 constexpr uint32_t kOffQ = 0;                                   // Q0, Q1
 constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;         // K ring
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;         // V ring
-constexpr uint32_t kOffT = kOffV + kStages * kTileBytes;         // table halves (2)
-constexpr uint32_t kOffBar = kOffT + 2 * kTableHalfBytes;        // mbarriers
+constexpr uint32_t kOffStage = kOffV + kStages * kTileBytes;     // one buffer per softmax warp
+constexpr uint32_t kOffBar = kOffStage + 8 * kStageWarpBytes;     // mbarriers
 // barrier indices
 constexpr int kBarQRaw = 0;
 constexpr int kBarQFull = 1;
@@ -101,9 +101,7 @@ constexpr int kBarKFull = kBarKRaw + kStages;
 constexpr int kBarKEmpty = kBarKFull + kStages;
 constexpr int kBarVFull = kBarKEmpty + kStages;
 constexpr int kBarVEmpty = kBarVFull + kStages;
-constexpr int kBarTFull = kBarVEmpty + kStages;  // + table buffer
-constexpr int kBarTEmpty = kBarTFull + 2;
-constexpr int kBarSFull = kBarTEmpty + 2;  // + q tile
+constexpr int kBarSFull = kBarVEmpty + kStages;  // + q tile
 constexpr int kBarPFull = kBarSFull + kQTiles;
 constexpr int kBarODone = kBarPFull + kQTiles;
 constexpr int kBarOFree = kBarODone + kQTiles;  // epilogue done reading O_t
@@ -122,9 +120,9 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
-constexpr uint32_t kRegsSoftmax = 168;
-constexpr uint32_t kRegsCopyMma = 88;  // WG0: producers, MMA issuer
-constexpr uint32_t kRegsRope = 88;
+constexpr uint32_t kRegsSoftmax = 176;
+constexpr uint32_t kRegsCopyMma = 80;  // WG0: producers, MMA issuer
+constexpr uint32_t kRegsRope = 80;
 static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -160,16 +158,15 @@ __device__ __forceinline__ void reg_dec() {
 }
 
 // 128 RoPE threads rotate rows [64 half, 64 half + 64) of a swizzled tile in
-// place with the table half at `tbl` ([64 rows][64 pairs] uint32). Thread u
-// owns 16-byte column chunk u & 15 (channel pairs 4(u&15) .. +3) of every
-// 8th row.
-// With kPublish, every rotated row whose token is below `rows_valid` (counted
-// from the tile's first row) is also stored to global memory at
-// grow + row * row_stride (bf16 elements, row 0 = the tile's first token).
+// place. The (cos, sin) words of tile row r are read from global memory at
+// tab + r * kPairs; rows at or beyond rows_valid (zeros in the tile) read no
+// table and stay zero. Thread u owns 16-byte column chunk u & 15 (channel
+// pairs 4(u&15) .. +3) of every 8th row. With kPublish the rotated rows below
+// rows_valid also go to global memory at grow + r * row_stride.
 template <bool kPublish = false>
-__device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u,
-                                            uint16_t *grow = nullptr, int64_t row_stride = 0,
-                                            int rows_valid = 0) {
+__device__ __forceinline__ void rotate_half(uint32_t tile, const uint32_t *tab, int half, int u,
+                                            int rows_valid, uint16_t *grow = nullptr,
+                                            int64_t row_stride = 0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
   // two batches of four rows: all loads of a batch in flight together
@@ -178,21 +175,21 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
     uint4 w[4], cs[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int rh = (i0 + i) * 8 + rsub;
-      w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
-      cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
+      const int r = half * 64 + (i0 + i) * 8 + rsub;
+      w[i] = ld_shared_v4(tile + sw128_offset(r, c16));
+      cs[i] = r < rows_valid ? ld_global_nc_v4(tab + static_cast<int64_t>(r) * kPairs + c16 * 4)
+                             : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int rh = (i0 + i) * 8 + rsub;
+      const int r = half * 64 + (i0 + i) * 8 + rsub;
       uint4 o;
       o.x = rope_pair(w[i].x, cs[i].x);
       o.y = rope_pair(w[i].y, cs[i].y);
       o.z = rope_pair(w[i].z, cs[i].z);
       o.w = rope_pair(w[i].w, cs[i].w);
-      st_shared_v4(tile + sw128_offset(half * 64 + rh, c16), o);
-      if (kPublish && half * 64 + rh < rows_valid)
-        st_global_v4(grow + (half * 64 + rh) * row_stride + c16 * 8, o);
+      st_shared_v4(tile + sw128_offset(r, c16), o);
+      if (kPublish && r < rows_valid) st_global_v4(grow + r * row_stride + c16 * 8, o);
     }
   }
 }
@@ -234,7 +231,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
 }
 
 struct Maps {
-  CUtensorMap q, k, v, table, krot, qrot;
+  CUtensorMap q, k, v, out, krot, qrot;
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -315,10 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(kBarVFull + s), 1);
       mbar_init(bar(kBarVEmpty + s), 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(kBarTFull + i), 1);
-      mbar_init(bar(kBarTEmpty + i), 4);
-    }
     for (int t = 0; t < kQTiles; ++t) {
       mbar_init(bar(kBarSFull + t), 1);
       mbar_init(bar(kBarPFull + t), 4);
@@ -350,30 +343,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     reg_dec<kRegsCopyMma>();
     if (warp == 0 && lane == 0) {
-      // ------------------------------------- producer: Q, K and the table
+      // ---------------------------------------------- producer: Q and K
       // Every copy that needs rotating is announced to the RoPE warps through
-      // the work queue (before its table halves, which the RoPE warps free);
-      // already rotated tiles go straight to the MMA.
+      // the work queue; already rotated tiles go straight to the MMA.
       tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.k);
-      tma_prefetch_desc(&maps.table);
       if (share) {
         tma_prefetch_desc(&maps.krot);
         tma_prefetch_desc(&maps.qrot);
       }
-      int g = 0;   // table halves issued so far
       int jt = 0;  // K tiles issued so far (all items)
       int pq = 0;  // queue entries posted so far
       bool ok = true;
-      auto table_half = [&](int row0) {
-        const int buf = g & 1;
-        const uint32_t use = static_cast<uint32_t>(g >> 1);
-        if (!(ok = mbar_wait(bar(kBarTEmpty + buf), (use & 1u) ^ 1u, abort_flag))) return;
-        mbar_arrive_expect_tx(bar(kBarTFull + buf), kTableHalfBytes);
-        tma_load_2d(sbase + kOffT + buf * kTableHalfBytes, &maps.table, bar(kBarTFull + buf), 0,
-                    row0);
-        ++g;
-      };
       auto post = [&](uint32_t x, uint32_t y) {
         const int e = pq % kRopeQ;
         const uint32_t use = static_cast<uint32_t>(pq / kRopeQ);
@@ -427,17 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           post(kRqQ | (last_q_parity << 8), static_cast<uint32_t>(item));
           ++q_local;
-          for (int i = 0; ok && i < 2 * kQTiles; ++i) table_half(m0 + i * static_cast<int>(kHalfRows));
         }
         const int j0 = first_tile(m0);
         const int prep_at = n_tiles > kPrepAtTile ? kPrepAtTile : n_tiles - 1;
         const uint64_t *fl_head =
             share ? kflags + (static_cast<int64_t>(b) * H + h) * n_tiles * 4 : nullptr;
+        int pieces = 0;  // prepare pieces posted for the next item, one per key tile
         for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
-          if (share && j == prep_at && next < n_items) {
-            post(kRqPrep, static_cast<uint32_t>(next));
-            if (!ok) break;
+          while (share && next < n_items && pieces < kPrepChunks &&
+                 (j >= prep_at + pieces || j == n_tiles - 1)) {
+            post(kRqPrep | (static_cast<uint32_t>(pieces) << 4), static_cast<uint32_t>(next));
+            ++pieces;
           }
+          if (!ok) break;
           const int s = jt % kStages;
           const int tj = tile_at(j0, j);
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
@@ -479,8 +462,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             post(kRqK | (static_cast<uint32_t>(s) << 4) | (par << 8) |
                      (static_cast<uint32_t>(tj) << 9),
                  static_cast<uint32_t>(item));
-            if (ok) table_half(tj * kBN);
-            if (ok) table_half(tj * kBN + static_cast<int>(kHalfRows));
           }
           // the next item's raw Q into L2 a few tiles before it is loaded (with
           // the exchange buffer the RoPE warps have read it long before)
@@ -504,8 +485,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           drain_wait(bar(((last_k_full >> sj) & 1u) ? kBarKFull + sj : kBarKRaw + sj),
                      (last_k_par >> sj) & 1u);
         }
-        for (int gg = (g > 2 ? g - 2 : 0); gg < g; ++gg)
-          drain_wait(bar(kBarTFull + (gg & 1)), static_cast<uint32_t>(gg >> 1) & 1u);
       }
     } else if (warp == 3 && lane == 0) {
       // ------------------------------------------------------ producer: V
@@ -717,99 +696,106 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: wait for the item's last P V, normalise, store bf16 rows
       if (!(ok = mbar_wait_warp(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
       tc_fence_after_sync();
+      // Each warp stages its 32 rows, 64 channels at a time, in its own
+      // 128-byte-swizzled buffer and lane 0 stores them with one TMA copy
+      // (rows past the sequence end are not written).
       const float inv_l = 1.f / l_run;
-      const int64_t token = static_cast<int64_t>(m0) + t * kBM + row;
-      const int64_t head0 = (static_cast<int64_t>(b) * S * H + h) * kD;
-      uint16_t *orow = out + head0 + token * row_stride;
+      const uint32_t stage = sbase + kOffStage + static_cast<uint32_t>(warp - 4) * kStageWarpBytes;
+      const int row0 = m0 + t * kBM + wq * 32;
+#pragma unroll 1
+      for (int c = 0; c < kD / 64; ++c) {
+        if (lane == 0) bulk_wait_read_all();  // the previous copy has read the buffer
+        __syncwarp();
 #pragma unroll
-      for (int c = 0; c < kD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(tO + c * 32, o);
-        tmem_ld_wait();
-        if (token < S) {
+        for (int hh = 0; hh < 2; ++hh) {  // 32 channels: 16-byte chunks 4 hh .. 4 hh + 3
+          uint32_t o[32];
+          tmem_ld32(tO + c * 64 + hh * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; i += 8) {
+          for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[i]) * inv_l, __uint_as_float(o[i + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[i + 2]) * inv_l, __uint_as_float(o[i + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[i + 4]) * inv_l, __uint_as_float(o[i + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[i + 6]) * inv_l, __uint_as_float(o[i + 7]) * inv_l);
-            *reinterpret_cast<uint4 *>(orow + c * 32 + i) = w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l,
+                              __uint_as_float(o[8 * q + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l,
+                              __uint_as_float(o[8 * q + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l,
+                              __uint_as_float(o[8 * q + 7]) * inv_l);
+            st_shared_v4(stage + lane * 128 + (((4 * hh + q) ^ (lane & 7)) << 4), w);
           }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < S) {
+          tma_store_4d(&maps.out, stage, c * 64, h, row0, b);
+          bulk_commit();
         }
       }
       tc_fence_before_sync();
       warp_arrive(bar(kBarOFree + t), lane);
     }
+    if (lane == 0) bulk_wait_all();  // every output store is complete
   } else {
     // --------------------------------------------------------- RoPE warps
     reg_dec<kRegsRope>();
     const int u = tid - 384;
-    int g = 0;  // table halves consumed so far
     bool ok = true;
-    // Rotates a landed tile in place; with `grow` (K tiles when sharing) the
-    // rotated rows also go to the exchange buffer.
-    auto rotate_tile = [&](uint32_t tile, uint16_t *grow, int rows_valid) {
-      for (int half = 0; ok && half < 2; ++half) {
-        const int buf = g & 1;
-        if (!(ok = mbar_wait_warp(bar(kBarTFull + buf), static_cast<uint32_t>(g >> 1) & 1u, abort_flag)))
-          return;
-        const uint32_t tbl = sbase + kOffT + buf * kTableHalfBytes;
+    // Rotates a landed tile whose first row is token tok0 in place; with
+    // `grow` (K tiles when sharing) the rotated rows also go to the exchange
+    // buffer.
+    auto rotate_tile = [&](uint32_t tile, int64_t tok0, uint16_t *grow) {
+      const uint32_t *tab = tabg + tok0 * kPairs;
+      const int rows_valid = static_cast<int>(S - tok0 < kBN ? (S - tok0 > 0 ? S - tok0 : 0) : kBN);
+      for (int half = 0; half < 2; ++half) {
         if (grow != nullptr)
-          rotate_half<true>(tile, tbl, half, u, grow, row_stride, rows_valid);
+          rotate_half<true>(tile, tab, half, u, rows_valid, grow, row_stride);
         else
-          rotate_half(tile, tbl, half, u);
-        warp_arrive(bar(kBarTEmpty + buf), lane);
-        ++g;
+          rotate_half(tile, tab, half, u, rows_valid);
       }
     };
-    // Prepares the CTA's next item while the current one runs: its Q rows and
-    // its first two K tiles rotated into the exchange buffer (the K tiles
-    // also published for other CTAs: a tile someone already published is
-    // rewritten with the same bytes), then Q-prep, after which the producer
-    // loads all three without reading flags.
-    auto prepare_next = [&](int next) {
+    // Prepares piece c of the CTA's next item while the current one runs:
+    // pieces 0-3 are its Q rows in 64-row blocks, rotated into the exchange
+    // buffer; pieces 4-7 the two 64-row halves of its first two K tiles,
+    // rotated into the exchange buffer and published (a tile someone already
+    // published is rewritten with the same bytes). After the last piece each
+    // warp arrives on Q-prep, after which the producer loads the Q rows and
+    // the two K tiles without reading flags. Small pieces keep raw K tiles
+    // from waiting long behind this work.
+    auto prepare_piece = [&](int next, int c) {
       int nb, nh, nm0;
       decode(next, nb, nh, nm0);
-      const int nj0 = first_tile(nm0);
-      // job 0: the Q rows; jobs 1, 2: the first two K tiles (one call site
-      // of the rotation keeps the RoPE warps' register budget)
-#pragma unroll 1
-      for (int job = 0; job < 3; ++job) {
+      const int kt = (c - 4) >> 1;  // K tile (0 or 1) of pieces 4-7
+      if (c < 4 || kt < n_tiles) {
         int64_t tok0;
-        int nrows;
         const uint16_t *src;
         uint16_t *dst;
-        uint64_t *fl = nullptr;
-        if (job == 0) {
-          tok0 = nm0;
-          nrows = static_cast<int>(S - tok0 < kRowsPerCta ? S - tok0 : kRowsPerCta);
-          const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
-          src = qg + o;
-          dst = qrot + o;
+        if (c < 4) {
+          tok0 = static_cast<int64_t>(nm0) + c * 64;
+          src = qg;
+          dst = qrot;
         } else {
-          if (job - 1 >= n_tiles) break;
-          const int tj = tile_at(nj0, job - 1);
-          fl = kflags + ((static_cast<int64_t>(nb) * H + nh) * n_tiles + tj) * 4;
-          tok0 = static_cast<int64_t>(tj) * kBN;
-          nrows = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
-          const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
-          src = kg + o;
-          dst = krot + o;
+          tok0 = static_cast<int64_t>(tile_at(first_tile(nm0), kt)) * kBN + ((c - 4) & 1) * 64;
+          src = kg;
+          dst = krot;
         }
-        rotate_rows_global(src, dst, tabg + tok0 * kPairs, nrows, row_stride, u);
+        const int nrows = static_cast<int>(S - tok0 < 64 ? (S - tok0 > 0 ? S - tok0 : 0) : 64);
+        const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
+        if (nrows > 0)
+          rotate_rows_global(src + o, dst + o, tabg + tok0 * kPairs, nrows, row_stride, u);
         fence_proxy_async_global();  // read by TMA copies
-        if (job > 0) {
+        if (c >= 4 && ((c - 4) & 1) == 1) {
           // publish as the in-place path does: this warp's rows, then its flag
+          const int tj = tile_at(first_tile(nm0), kt);
           fence_acq_rel_gpu();
           __syncwarp();
           if (lane == 0) {
             fence_acq_rel_gpu();
-            st_relaxed_gpu_u64(fl + (u >> 5), token);
+            st_relaxed_gpu_u64(
+                kflags + ((static_cast<int64_t>(nb) * H + nh) * n_tiles + tj) * 4 + (u >> 5), token);
           }
         }
       }
-      warp_arrive(bar(kBarQPrep), lane);
+      if (c == kPrepChunks - 1) warp_arrive(bar(kBarQPrep), lane);
     };
     // Work comes from the producer's queue in issue order; every rotation
     // step, the table ring and each wait are this warp's alone (one arrival
@@ -828,14 +814,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kind == kRqEnd) break;
       const int item = static_cast<int>(y);
       if (kind == kRqPrep) {
-        prepare_next(item);
+        prepare_piece(item, static_cast<int>((x >> 4) & 15u));
         continue;
       }
       const uint32_t par = (x >> 8) & 1u;
       if (kind == kRqQ) {
         if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
-        for (int t = 0; ok && t < kQTiles; ++t) rotate_tile(sbase + kOffQ + t * kTileBytes, nullptr, 0);
-        if (!ok) break;
+        int b, h, m0;
+        decode(item, b, h, m0);
+        for (int t = 0; t < kQTiles; ++t)
+          rotate_tile(sbase + kOffQ + t * kTileBytes, static_cast<int64_t>(m0) + t * kBM, nullptr);
         fence_proxy_async_smem();
         warp_arrive(bar(kBarQFull), lane);
         continue;
@@ -848,9 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
       const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
       uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
-      const int rows_valid = static_cast<int>(S - tok0 < kBN ? S - tok0 : kBN);
-      rotate_tile(sbase + kOffK + s * kTileBytes, grow, rows_valid);
-      if (!ok) break;
+      rotate_tile(sbase + kOffK + s * kTileBytes, tok0, grow);
       fence_proxy_async_smem();
       if (share) {
         // publish this warp's rows of tile tj: each lane's stores, then
@@ -897,9 +883,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// q, k or v as a 4-D tensor (D, H, S, B); one box = 64 channels x 128 tokens
-// of one head, 128-byte swizzled; out-of-range tokens read as zeros.
-bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H) {
+// q, k, v or out as a 4-D tensor (D, H, S, B); one box = 64 channels x
+// box_rows tokens of one head, 128-byte swizzled; out-of-range tokens read as
+// zeros and are not written.
+bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H,
+                   uint32_t box_rows = kBN) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
@@ -907,23 +895,10 @@ bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H) {
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
                                  static_cast<cuuint64_t>(H) * kD * 2,
                                  static_cast<cuuint64_t>(S) * H * kD * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBN), 1};
+  const cuuint32_t box[4] = {64, 1, box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// The packed table [S, 64] uint32 as a 2-D tensor; one box = 64 tokens.
-bool make_table_map(CUtensorMap *map, const uint32_t *table, int64_t S) {
-  EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPairs), static_cast<cuuint64_t>(S)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kPairs) * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kPairs), kHalfRows};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(table), dims, strides,
-            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -965,7 +940,7 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (attr_err != cudaSuccess) return attr_err;
   Maps maps;
   if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
-      !make_head_map(&maps.v, v, B, S, H) || !make_table_map(&maps.table, table, S))
+      !make_head_map(&maps.v, v, B, S, H) || !make_head_map(&maps.out, out, B, S, H, 32))
     return cudaErrorInvalidValue;
   uint64_t *kflags = nullptr;
   uint16_t *krot = nullptr, *qrot = nullptr;

@@ -120,6 +120,28 @@ __device__ __forceinline__ void tma_prefetch_l2_4d(const void *tmap, int c0, int
       : "memory");
 }
 
+// Tile store shared -> global (bulk-group completion): one 4-D box from the
+// tensor map at the given coordinates; rows outside the tensor are not
+// written. Commit, then wait for the copies of this thread's groups to have
+// read shared memory (.read) or to be complete.
+__device__ __forceinline__ void tma_store_4d(const void *tmap, uint32_t src, int c0, int c1, int c2,
+                                             int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 // ------------------------------------------------------ tensor memory (TMEM)
 
 // Warp-wide: allocate `ncols` TMEM columns, the base address goes to smem.
