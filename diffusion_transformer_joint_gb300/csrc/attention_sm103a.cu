@@ -75,7 +75,9 @@ constexpr int kStages = 2;  // K and V ring depth
 constexpr int kPairs = kD / 2;
 constexpr uint32_t kTileBytes = 128 * 128 * 2;
 constexpr uint32_t kBlockBytes = 16384;          // one 64-channel swizzle block
-constexpr uint32_t kStageWarpBytes = 32 * 128;  // epilogue staging: 32 rows x 64 channels bf16
+constexpr uint32_t kStageWarpBytes = 32 * 64;  // epilogue staging: 32 rows x 32 channels bf16
+constexpr uint32_t kTableRows = 64;              // table rows per shared-memory table load
+constexpr uint32_t kTableBytes = kTableRows * kPairs * 4;  // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr int kQPrefetchTiles = 6;  // key tiles before an item's end its successor's Q is prefetched
@@ -92,7 +94,8 @@ constexpr uint32_t kOffQ = 0;                                   // Q0, Q1
 constexpr uint32_t kOffK = kOffQ + kQTiles * kTileBytes;         // K ring
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;         // V ring
 constexpr uint32_t kOffStage = kOffV + kStages * kTileBytes;     // one buffer per softmax warp
-constexpr uint32_t kOffBar = kOffStage + 8 * kStageWarpBytes;     // mbarriers
+constexpr uint32_t kOffT = kOffStage + 8 * kStageWarpBytes;       // table rows for in-place RoPE
+constexpr uint32_t kOffBar = kOffT + kTableBytes;                 // mbarriers
 // barrier indices
 constexpr int kBarQRaw = 0;
 constexpr int kBarQFull = 1;
@@ -101,7 +104,9 @@ constexpr int kBarKFull = kBarKRaw + kStages;
 constexpr int kBarKEmpty = kBarKFull + kStages;
 constexpr int kBarVFull = kBarKEmpty + kStages;
 constexpr int kBarVEmpty = kBarVFull + kStages;
-constexpr int kBarSFull = kBarVEmpty + kStages;  // + q tile
+constexpr int kBarTFull = kBarVEmpty + kStages;  // table buffer loaded
+constexpr int kBarTEmpty = kBarTFull + 1;         // every RoPE warp done with it
+constexpr int kBarSFull = kBarTEmpty + 1;         // + q tile
 constexpr int kBarPFull = kBarSFull + kQTiles;
 constexpr int kBarODone = kBarPFull + kQTiles;
 constexpr int kBarOFree = kBarODone + kQTiles;  // epilogue done reading O_t
@@ -120,9 +125,9 @@ constexpr uint32_t kSmemBytes = kSmemUsed + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
-constexpr uint32_t kRegsSoftmax = 176;
-constexpr uint32_t kRegsCopyMma = 80;  // WG0: producers, MMA issuer
-constexpr uint32_t kRegsRope = 80;
+constexpr uint32_t kRegsSoftmax = 168;
+constexpr uint32_t kRegsCopyMma = 88;  // WG0: producers, MMA issuer
+constexpr uint32_t kRegsRope = 88;
 static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -158,14 +163,14 @@ __device__ __forceinline__ void reg_dec() {
 }
 
 // 128 RoPE threads rotate rows [64 half, 64 half + 64) of a swizzled tile in
-// place. The (cos, sin) words of tile row r are read from global memory at
-// tab + r * kPairs; rows at or beyond rows_valid (zeros in the tile) read no
-// table and stay zero. Thread u owns 16-byte column chunk u & 15 (channel
-// pairs 4(u&15) .. +3) of every 8th row. With kPublish the rotated rows below
+// place with the (cos, sin) words of those rows at `tbl` in shared memory
+// ([64 rows][64 pairs] uint32; rows past the sequence end hold zeros, as do
+// the tile's). Thread u owns 16-byte column chunk u & 15 (channel pairs
+// 4(u&15) .. +3) of every 8th row. With kPublish the rotated rows below
 // rows_valid also go to global memory at grow + r * row_stride.
 template <bool kPublish = false>
-__device__ __forceinline__ void rotate_half(uint32_t tile, const uint32_t *tab, int half, int u,
-                                            int rows_valid, uint16_t *grow = nullptr,
+__device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u,
+                                            int rows_valid = 0, uint16_t *grow = nullptr,
                                             int64_t row_stride = 0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
@@ -175,10 +180,9 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, const uint32_t *tab, 
     uint4 w[4], cs[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int r = half * 64 + (i0 + i) * 8 + rsub;
-      w[i] = ld_shared_v4(tile + sw128_offset(r, c16));
-      cs[i] = r < rows_valid ? ld_global_nc_v4(tab + static_cast<int64_t>(r) * kPairs + c16 * 4)
-                             : make_uint4(0u, 0u, 0u, 0u);
+      const int rh = (i0 + i) * 8 + rsub;
+      w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
+      cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -231,7 +235,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
 }
 
 struct Maps {
-  CUtensorMap q, k, v, out, krot, qrot;
+  CUtensorMap q, k, v, out, krot, qrot, table;
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -320,6 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(kBarQFree), 1);
     mbar_init(bar(kBarQPrep), 4);
+    mbar_init(bar(kBarTFull), 1);
+    mbar_init(bar(kBarTEmpty), 4);
     for (int e = 0; e < kRopeQ; ++e) {
       mbar_init(bar(kBarRQFull + e), 1);
       mbar_init(bar(kBarRQEmpty + e), 4);
@@ -696,38 +702,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       // epilogue: wait for the item's last P V, normalise, store bf16 rows
       if (!(ok = mbar_wait_warp(bar(kBarODone + t), static_cast<uint32_t>(jt - 1) & 1u, abort_flag))) break;
       tc_fence_after_sync();
-      // Each warp stages its 32 rows, 64 channels at a time, in its own
-      // 128-byte-swizzled buffer and lane 0 stores them with one TMA copy
+      // Each warp stages its 32 rows, 32 channels at a time, in its own
+      // 64-byte-swizzled 2 KB buffer and lane 0 stores them with one TMA copy
       // (rows past the sequence end are not written).
       const float inv_l = 1.f / l_run;
       const uint32_t stage = sbase + kOffStage + static_cast<uint32_t>(warp - 4) * kStageWarpBytes;
       const int row0 = m0 + t * kBM + wq * 32;
 #pragma unroll 1
-      for (int c = 0; c < kD / 64; ++c) {
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait();
         if (lane == 0) bulk_wait_read_all();  // the previous copy has read the buffer
         __syncwarp();
+        // 16-byte chunk q of row `lane` sits at chunk q ^ ((lane >> 1) & 3)
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {  // 32 channels: 16-byte chunks 4 hh .. 4 hh + 3
-          uint32_t o[32];
-          tmem_ld32(tO + c * 64 + hh * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
-            w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l,
-                              __uint_as_float(o[8 * q + 3]) * inv_l);
-            w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l,
-                              __uint_as_float(o[8 * q + 5]) * inv_l);
-            w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l,
-                              __uint_as_float(o[8 * q + 7]) * inv_l);
-            st_shared_v4(stage + lane * 128 + (((4 * hh + q) ^ (lane & 7)) << 4), w);
-          }
+        for (int q = 0; q < 4; ++q) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[8 * q]) * inv_l, __uint_as_float(o[8 * q + 1]) * inv_l);
+          w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
+          w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
+          w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
+          st_shared_v4(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && row0 < S) {
-          tma_store_4d(&maps.out, stage, c * 64, h, row0, b);
+          tma_store_4d(&maps.out, stage, c * 32, h, row0, b);
           bulk_commit();
         }
       }
@@ -740,17 +741,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_dec<kRegsRope>();
     const int u = tid - 384;
     bool ok = true;
+    int tuse = 0;   // table-buffer halves consumed so far
+    int tload = 0;  // table-buffer loads issued (RoPE warp 0)
+    // Table rows [row0, row0 + 64) into the shared buffer: RoPE warp 0 loads
+    // them once every RoPE warp is done with the previous rows.
+    auto load_table = [&](int64_t row0) {
+      if (u < 32) {
+        if (!(ok = mbar_wait_warp(bar(kBarTEmpty), (static_cast<uint32_t>(tuse) & 1u) ^ 1u,
+                                  abort_flag)))
+          return;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
+          tma_load_2d(sbase + kOffT, &maps.table, bar(kBarTFull), 0, static_cast<int>(row0));
+        }
+        __syncwarp();
+        ++tload;
+      }
+    };
     // Rotates a landed tile whose first row is token tok0 in place; with
     // `grow` (K tiles when sharing) the rotated rows also go to the exchange
-    // buffer.
+    // buffer. The table rows of its first half were requested already.
     auto rotate_tile = [&](uint32_t tile, int64_t tok0, uint16_t *grow) {
-      const uint32_t *tab = tabg + tok0 * kPairs;
       const int rows_valid = static_cast<int>(S - tok0 < kBN ? (S - tok0 > 0 ? S - tok0 : 0) : kBN);
-      for (int half = 0; half < 2; ++half) {
+      for (int half = 0; ok && half < 2; ++half) {
+        if (!(ok = mbar_wait_warp(bar(kBarTFull), static_cast<uint32_t>(tuse) & 1u, abort_flag)))
+          return;
         if (grow != nullptr)
-          rotate_half<true>(tile, tab, half, u, rows_valid, grow, row_stride);
+          rotate_half<true>(tile, sbase + kOffT, half, u, rows_valid, grow, row_stride);
         else
-          rotate_half(tile, tab, half, u, rows_valid);
+          rotate_half(tile, sbase + kOffT, half, u);
+        warp_arrive(bar(kBarTEmpty), lane);
+        ++tuse;
+        if (half == 0) load_table(tok0 + 64);
       }
     };
     // Prepares piece c of the CTA's next item while the current one runs:
@@ -819,11 +841,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint32_t par = (x >> 8) & 1u;
       if (kind == kRqQ) {
-        if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
         int b, h, m0;
         decode(item, b, h, m0);
-        for (int t = 0; t < kQTiles; ++t)
+        load_table(m0);
+        if (!ok) break;
+        if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
+        for (int t = 0; ok && t < kQTiles; ++t) {
+          if (t > 0) load_table(static_cast<int64_t>(m0) + t * kBM);
           rotate_tile(sbase + kOffQ + t * kTileBytes, static_cast<int64_t>(m0) + t * kBM, nullptr);
+        }
+        if (!ok) break;
         fence_proxy_async_smem();
         warp_arrive(bar(kBarQFull), lane);
         continue;
@@ -833,10 +860,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tj = static_cast<int>(x >> 9);
       int b, h, m0;
       decode(item, b, h, m0);
-      if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
       const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
+      load_table(tok0);  // in flight while the tile itself lands
+      if (!ok) break;
+      if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
       uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
       rotate_tile(sbase + kOffK + s * kTileBytes, tok0, grow);
+      if (!ok) break;
       fence_proxy_async_smem();
       if (share) {
         // publish this warp's rows of tile tj: each lane's stores, then
@@ -852,6 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       warp_arrive(bar(kBarKFull + s), lane);
     }
+    // a table copy still in flight after an abort lands before the CTA exits
+    if (u < 32 && tload > tuse) drain_wait(bar(kBarTFull), static_cast<uint32_t>(tload - 1) & 1u);
   }
 
   tc_fence_before_sync();
@@ -883,11 +915,12 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// q, k, v or out as a 4-D tensor (D, H, S, B); one box = 64 channels x
-// box_rows tokens of one head, 128-byte swizzled; out-of-range tokens read as
-// zeros and are not written.
+// q, k, v or out as a 4-D tensor (D, H, S, B); one box = box_ch channels x
+// box_rows tokens of one head, swizzled 128 bytes (64-channel boxes) or 64
+// bytes (32-channel boxes); out-of-range tokens read as zeros and are not
+// written.
 bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H,
-                   uint32_t box_rows = kBN) {
+                   uint32_t box_rows = kBN, uint32_t box_ch = 64) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return false;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(H),
@@ -895,10 +928,24 @@ bool make_head_map(CUtensorMap *map, const void *x, int B, int64_t S, int H,
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(kD) * 2,
                                  static_cast<cuuint64_t>(H) * kD * 2,
                                  static_cast<cuuint64_t>(S) * H * kD * 2};
-  const cuuint32_t box[4] = {64, 1, box_rows, 1};
+  const cuuint32_t box[4] = {box_ch, 1, box_rows, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(x), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            box_ch == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The packed table [S, 64] uint32 as a 2-D tensor; one box = 64 tokens.
+bool make_table_map(CUtensorMap *map, const uint32_t *table, int64_t S) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kPairs), static_cast<cuuint64_t>(S)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kPairs) * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kPairs), kTableRows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(table), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -940,7 +987,8 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (attr_err != cudaSuccess) return attr_err;
   Maps maps;
   if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
-      !make_head_map(&maps.v, v, B, S, H) || !make_head_map(&maps.out, out, B, S, H, 32))
+      !make_head_map(&maps.v, v, B, S, H) || !make_head_map(&maps.out, out, B, S, H, 32, 32) ||
+      !make_table_map(&maps.table, table, S))
     return cudaErrorInvalidValue;
   uint64_t *kflags = nullptr;
   uint16_t *krot = nullptr, *qrot = nullptr;
