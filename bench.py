@@ -359,7 +359,8 @@ def _oracle_inputs(w):
 def _rows_for(w, seconds, threads, inputs):
     import numpy as np
 
-    probe = np.arange(0, w.S, max(1, w.S // 16), dtype=np.int64)[:16]
+    probe = np.arange(0, w.S, max(1, w.S // 32), dtype=np.int64)[:32]
+    _oracle_sample(w, probe[:4], threads, *inputs)  # warm: threads, caches, page faults
     t = _oracle_sample(w, probe, threads, *inputs)
     per_row = t / probe.size
     n = int(max(16, min(w.S, seconds / max(per_row, 1e-9))))
