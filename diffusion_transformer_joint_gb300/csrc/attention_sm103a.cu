@@ -80,6 +80,7 @@ constexpr uint32_t kTableRows = 64;              // table rows per shared-memory
 constexpr uint32_t kTableBytes = kTableRows * kPairs * 4;  // 16 KB
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr int kVPrefetch = 2;       // V tiles ahead of the copy that are prefetched into L2
 constexpr int kQPrefetchTiles = 6;  // key tiles before an item's end its successor's Q is prefetched
 constexpr int kPrepAtTile = 2;      // key tile of an item from which the next one is prepared
 constexpr int kPrepChunks = 8;      // 64-row pieces: 4 of Q, 2 per K tile for the first two K tiles
@@ -510,6 +511,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
           tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, tj * kBN, b);
           tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, tj * kBN, b);
+          // the tile two ahead into L2 now, so that its copy does not wait on
+          // DRAM when the ring frees up
+          if (j + kVPrefetch < n_tiles) {
+            const int tp = tile_at(j0, j + kVPrefetch);
+            tma_prefetch_l2_4d(&maps.v, 0, h, tp * kBN, b);
+            tma_prefetch_l2_4d(&maps.v, 64, h, tp * kBN, b);
+          }
         }
       }
       // every copy issued above has landed before the CTA exits (a no-op
