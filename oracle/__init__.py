@@ -18,7 +18,10 @@ norms, the post-RoPE dot product depends only on the id difference, the
 per-axis frequencies match theta^(-2j/d_a) evaluated independently at high
 precision, a complex-number brute force agrees, identical keys give the mean
 of V, and the attention agrees with torch's float64 SDPA and with a naive
-Python triple loop on tiny inputs. No function is "parity unpinned".
+Python triple loop on tiny inputs. The optional QK RMS normalisation agrees
+with torch's float64 rms_norm and with its closed-form mean square, and the
+normalised attention with SDPA on inputs normalised and rotated separately.
+No function is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -89,6 +92,14 @@ class Oracle:
             P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
             P, P, ctypes.c_int, ctypes.c_double, P, ctypes.c_int64, ctypes.c_int, P]
         lib.oracle_joint_rope_attention.restype = ctypes.c_int
+        lib.oracle_rms_norm.argtypes = [P, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                        ctypes.c_int, P, ctypes.c_double, P]
+        lib.oracle_rms_norm.restype = None
+        lib.oracle_joint_qknorm_rope_attention.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+            P, P, ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int64, ctypes.c_double,
+            P, ctypes.c_int64, ctypes.c_int, P]
+        lib.oracle_joint_qknorm_rope_attention.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -118,12 +129,24 @@ class Oracle:
         self.lib.oracle_rope_apply(_ptr(x), B, S, H, D, _ptr(cos_t), _ptr(sin_t), _ptr(y))
         return y
 
+    def rms_norm(self, x, w, eps=1e-6):
+        """RMS-normalise every head vector of x [B, S, H, D] with weights w [D] (fp64)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        B, S, H, D = x.shape
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        assert w.shape == (D,)
+        y = np.empty_like(x)
+        self.lib.oracle_rms_norm(_ptr(x), B, S, H, D, _ptr(w), float(eps), _ptr(y))
+        return y
+
     def joint_rope_attention(self, q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                             theta=2000.0, rows=None, threads=None):
+                             theta=2000.0, rows=None, threads=None, qk_norm=None):
         """out[b, r, h, :] for the query tokens ``rows`` (all when None).
 
         q, k, v: [B, S, H, D] arrays (any float dtype; converted exactly to fp64).
-        Returns fp64 [B, len(rows), H, D].
+        qk_norm: None, or (qw_txt, kw_txt, qw_img, kw_img, eps) with weights [D]:
+        Q and K are RMS-normalised (text tokens with the text weights) before
+        the rotation. Returns fp64 [B, len(rows), H, D].
         """
         q = np.ascontiguousarray(q, dtype=np.float64)
         k = np.ascontiguousarray(k, dtype=np.float64)
@@ -142,9 +165,19 @@ class Oracle:
         if rows_arr.size == 0:
             return out
         n_threads = int(threads) if threads else default_threads()
-        rc = self.lib.oracle_joint_rope_attention(
-            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
-            float(theta), _ptr(rows_arr), rows_arr.size, n_threads, _ptr(out))
+        if qk_norm is None:
+            rc = self.lib.oracle_joint_rope_attention(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), _ptr(rows_arr), rows_arr.size, n_threads, _ptr(out))
+        else:
+            *ws, eps = qk_norm
+            ws = [np.ascontiguousarray(w, dtype=np.float64) for w in ws]
+            assert all(w.shape == (D,) for w in ws)
+            s_txt = 0 if txt_ids is None else int(np.asarray(txt_ids).reshape(-1, axes.size).shape[0])
+            rc = self.lib.oracle_joint_qknorm_rope_attention(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), *[_ptr(w) for w in ws], s_txt, float(eps), _ptr(rows_arr),
+                rows_arr.size, n_threads, _ptr(out))
         if rc != 0:
             raise ValueError("oracle_joint_rope_attention: sum(axes_dims) must equal D, "
                              "sizes > 0")
@@ -167,7 +200,11 @@ def rope_apply(x, cos_t, sin_t):
     return default().rope_apply(x, cos_t, sin_t)
 
 
+def rms_norm(x, w, eps=1e-6):
+    return default().rms_norm(x, w, eps)
+
+
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                         theta=2000.0, rows=None, threads=None):
+                         theta=2000.0, rows=None, threads=None, qk_norm=None):
     return default().joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims, theta,
-                                          rows, threads)
+                                          rows, threads, qk_norm)

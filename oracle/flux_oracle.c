@@ -31,6 +31,17 @@
  *      non-causal, per batch element and head, d = head_dim = 128, with q^ and
  *      k^ the RoPE-rotated queries and keys; V is not rotated.
  *
+ *   4. Optional QK RMS normalisation before the rotation ("Diffusers 中
+ *      Flux2Transformer2DModel 全面解析", section "内部架构双流块与单流块": in
+ *      the joint attention Q and K are RMS-normalised right after their
+ *      projections, with separate norms for the text and the image stream;
+ *      section "并行化支持": the norm acts on the whole head_dim of a head;
+ *      section "模型配置参数全解": eps = 1e-6). For one head vector x[D] with
+ *      a learned per-channel weight w[D]:
+ *        y_c = x_c / sqrt(mean over c' of x_c'^2 + eps) * w_c,
+ *      text tokens (the first S_txt) with the text weights, the others with
+ *      the image weights; V is not normalised.
+ *
  * Layout: q, k, v, out are [B, S, H, D] row-major (D fastest), in double.
  * ids are [S, n_axes] int32 and are shared by every batch element.
  */
@@ -76,6 +87,23 @@ void oracle_rope_apply_vec(const double *x, const double *c, const double *sn,
   }
 }
 
+/* RMS normalisation of one head vector, step 4 above. */
+void oracle_rms_norm_vec(const double *x, const double *w, int D, double eps,
+                         double *y) {
+  double ss = 0.0;
+  for (int c = 0; c < D; ++c) ss += x[c] * x[c];
+  const double r = 1.0 / sqrt(ss / (double)D + eps);
+  for (int c = 0; c < D; ++c) y[c] = x[c] * r * w[c];
+}
+
+/* RMS normalisation of every head vector of a [B, S, H, D] tensor with one
+ * weight vector w[D]. */
+void oracle_rms_norm(const double *x, int B, int64_t S, int H, int D,
+                     const double *w, double eps, double *y) {
+  for (int64_t n = 0; n < (int64_t)B * S * H; ++n)
+    oracle_rms_norm_vec(x + n * D, w, D, eps, y + n * D);
+}
+
 /* Rotation of a whole [B, S, H, D] tensor with tables [S, D/2]. */
 void oracle_rope_apply(const double *x, int B, int64_t S, int H, int D,
                        const double *cos_t, const double *sin_t, double *y) {
@@ -92,6 +120,10 @@ void oracle_rope_apply(const double *x, int B, int64_t S, int H, int D,
 
 typedef struct {
   const double *q, *k, *v, *cos_t, *sin_t;
+  /* optional RMS-norm weights [D] (all NULL: no normalisation) */
+  const double *qw_txt, *kw_txt, *qw_img, *kw_img;
+  int64_t S_txt;
+  double eps;
   int B, H, D;
   int64_t S;
   const int64_t *rows; /* query token indices to evaluate */
@@ -110,15 +142,27 @@ static void attn_unit(attn_job *J, int b, int h) {
   double *khat = (double *)malloc(sizeof(double) * (size_t)S * D);
   double *z = (double *)malloc(sizeof(double) * (size_t)S);
   double *qhat = (double *)malloc(sizeof(double) * (size_t)D);
+  double *xn = (double *)malloc(sizeof(double) * (size_t)D);
+  const int norm = J->qw_txt != NULL;
   for (int64_t j = 0; j < S; ++j) {
     int64_t off = (((int64_t)b * S + j) * H + h) * D;
-    oracle_rope_apply_vec(J->k + off, J->cos_t + j * (D / 2),
+    const double *kj = J->k + off;
+    if (norm) {
+      oracle_rms_norm_vec(kj, j < J->S_txt ? J->kw_txt : J->kw_img, D, J->eps, xn);
+      kj = xn;
+    }
+    oracle_rope_apply_vec(kj, J->cos_t + j * (D / 2),
                           J->sin_t + j * (D / 2), D, khat + j * D);
   }
   for (int64_t r = 0; r < J->n_rows; ++r) {
     int64_t i = J->rows[r];
     int64_t qoff = (((int64_t)b * S + i) * H + h) * D;
-    oracle_rope_apply_vec(J->q + qoff, J->cos_t + i * (D / 2),
+    const double *qi = J->q + qoff;
+    if (norm) {
+      oracle_rms_norm_vec(qi, i < J->S_txt ? J->qw_txt : J->qw_img, D, J->eps, xn);
+      qi = xn;
+    }
+    oracle_rope_apply_vec(qi, J->cos_t + i * (D / 2),
                           J->sin_t + i * (D / 2), D, qhat);
     /* logits z_j = q^_i . k^_j / sqrt(D) */
     double zmax = -INFINITY;
@@ -146,6 +190,7 @@ static void attn_unit(attn_job *J, int b, int h) {
   free(khat);
   free(z);
   free(qhat);
+  free(xn);
 }
 
 static void *attn_worker(void *arg) {
@@ -165,11 +210,13 @@ static void *attn_worker(void *arg) {
  * already concatenated, [S, n_axes]. out is [B, n_rows, H, D]. Work over
  * (b, h) is spread on n_threads POSIX threads; the arithmetic of each output
  * does not depend on the thread count. Returns 0, or -1 on bad arguments. */
-int oracle_joint_rope_attention(const double *q, const double *k,
-                                const double *v, int B, int64_t S, int H, int D,
-                                const int32_t *ids, const int32_t *axes_dims,
-                                int n_axes, double theta, const int64_t *rows,
-                                int64_t n_rows, int n_threads, double *out) {
+static int joint_attention(const double *q, const double *k, const double *v,
+                           int B, int64_t S, int H, int D, const int32_t *ids,
+                           const int32_t *axes_dims, int n_axes, double theta,
+                           const double *qw_txt, const double *kw_txt,
+                           const double *qw_img, const double *kw_img,
+                           int64_t S_txt, double eps, const int64_t *rows,
+                           int64_t n_rows, int n_threads, double *out) {
   int sum = 0;
   for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
   if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0) return -1;
@@ -189,6 +236,8 @@ int oracle_joint_rope_attention(const double *q, const double *k,
   }
   attn_job J;
   J.q = q; J.k = k; J.v = v; J.cos_t = cos_t; J.sin_t = sin_t;
+  J.qw_txt = qw_txt; J.kw_txt = kw_txt; J.qw_img = qw_img; J.kw_img = kw_img;
+  J.S_txt = S_txt; J.eps = eps;
   J.B = B; J.H = H; J.D = D; J.S = S;
   J.rows = rows; J.n_rows = n_rows; J.out = out; J.next_unit = 0;
   pthread_mutex_init(&J.lock, NULL);
@@ -202,4 +251,29 @@ int oracle_joint_rope_attention(const double *q, const double *k,
   free(cos_t);
   free(sin_t);
   return 0;
+}
+
+int oracle_joint_rope_attention(const double *q, const double *k,
+                                const double *v, int B, int64_t S, int H, int D,
+                                const int32_t *ids, const int32_t *axes_dims,
+                                int n_axes, double theta, const int64_t *rows,
+                                int64_t n_rows, int n_threads, double *out) {
+  return joint_attention(q, k, v, B, S, H, D, ids, axes_dims, n_axes, theta, NULL,
+                         NULL, NULL, NULL, 0, 0.0, rows, n_rows, n_threads, out);
+}
+
+/* The same with the QK RMS normalisation of step 4 before the rotation:
+ * weights [D] for the text tokens (the first S_txt) and for the others. */
+int oracle_joint_qknorm_rope_attention(
+    const double *q, const double *k, const double *v, int B, int64_t S, int H,
+    int D, const int32_t *ids, const int32_t *axes_dims, int n_axes, double theta,
+    const double *qw_txt, const double *kw_txt, const double *qw_img,
+    const double *kw_img, int64_t S_txt, double eps, const int64_t *rows,
+    int64_t n_rows, int n_threads, double *out) {
+  if (qw_txt == NULL || kw_txt == NULL || qw_img == NULL || kw_img == NULL ||
+      S_txt < 0 || S_txt > S || !(eps >= 0.0))
+    return -1;
+  return joint_attention(q, k, v, B, S, H, D, ids, axes_dims, n_axes, theta, qw_txt,
+                         kw_txt, qw_img, kw_img, S_txt, eps, rows, n_rows, n_threads,
+                         out);
 }

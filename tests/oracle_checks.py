@@ -266,6 +266,71 @@ def check_rows_and_threads(orc):
     assert np.array_equal(sub, full1[:, rows])
 
 
+# ------------------------------------------------------ QK RMS normalisation
+
+
+def _torch_rms_norm(x, w, eps):
+    import torch
+
+    return torch.nn.functional.rms_norm(torch.from_numpy(x), (x.shape[-1],),
+                                        weight=torch.from_numpy(w), eps=eps).numpy()
+
+
+def check_rms_norm_mean_square(orc):
+    """With unit weights the output's mean square is ms / (ms + eps) exactly
+    (ms the input's mean square): 1 for large vectors, ms / eps for tiny ones."""
+    rng = _rng(16)
+    D = 128
+    for scale in (1.0, 30.0, 1e-4):
+        x = scale * rng.standard_normal((2, 7, 3, D))
+        y = orc.rms_norm(x, np.ones(D), 1e-6)
+        ms = (x * x).mean(axis=-1)
+        assert np.allclose((y * y).mean(axis=-1), ms / (ms + 1e-6), rtol=1e-13, atol=0)
+
+
+def check_rms_norm_vs_torch(orc):
+    """torch's float64 rms_norm (a library routine) on random weights."""
+    rng = _rng(17)
+    D = 128
+    w = rng.uniform(0.2, 2.0, D)
+    for scale, eps in ((1.0, 1e-6), (1e-3, 1e-6), (5.0, 0.5)):
+        x = scale * rng.standard_normal((1, 11, 2, D))
+        y = orc.rms_norm(x, w, eps)
+        assert np.allclose(y, _torch_rms_norm(x, w, eps), rtol=1e-13, atol=1e-15)
+
+
+def check_qk_norm_attention_vs_sdpa(orc):
+    """Attention with the QK norm: q and k normalised by torch's rms_norm with
+    the text weights on the text tokens and the image weights on the others,
+    rotated with complex exponentials, then torch's float64 SDPA."""
+    rng = _rng(18)
+    B, S_t, S_i, H, D = 1, 6, 27, 2, 128
+    S = S_t + S_i
+    txt, img = _rand_ids(rng, S_t), _rand_ids(rng, S_i)
+    ids = np.concatenate([txt, img])
+    q = 3.0 * rng.standard_normal((B, S, H, D))
+    k = 0.5 * rng.standard_normal((B, S, H, D))
+    v = rng.standard_normal((B, S, H, D))
+    qw_t, kw_t, qw_i, kw_i = (rng.uniform(0.3, 2.5, D) for _ in range(4))
+    eps = 1e-6
+    qn = np.concatenate([_torch_rms_norm(q[:, :S_t], qw_t, eps),
+                         _torch_rms_norm(q[:, S_t:], qw_i, eps)], axis=1)
+    kn = np.concatenate([_torch_rms_norm(k[:, :S_t], kw_t, eps),
+                         _torch_rms_norm(k[:, S_t:], kw_i, eps)], axis=1)
+    ref = _sdpa_f64(_rotate_all(qn, ids, FLUX_AXES, FLUX_THETA),
+                    _rotate_all(kn, ids, FLUX_AXES, FLUX_THETA), v)
+    out = orc.joint_rope_attention(q, k, v, txt, img, FLUX_AXES, FLUX_THETA, threads=2,
+                                   qk_norm=(qw_t, kw_t, qw_i, kw_i, eps))
+    assert np.allclose(out, ref, rtol=0, atol=1e-11), np.abs(out - ref).max()
+    # the norm removes any positive per-token scale of q and k (eps aside)
+    scl = rng.uniform(0.5, 4.0, (B, S, 1, 1))
+    out2 = orc.joint_rope_attention(q * scl, k / scl, v, txt, img, FLUX_AXES, FLUX_THETA,
+                                    qk_norm=(qw_t, kw_t, qw_i, kw_i, 0.0))
+    out3 = orc.joint_rope_attention(q, k, v, txt, img, FLUX_AXES, FLUX_THETA,
+                                    qk_norm=(qw_t, kw_t, qw_i, kw_i, 0.0))
+    assert np.allclose(out2, out3, rtol=0, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_zero_ids_identity,
     check_frequencies_high_precision,
@@ -281,4 +346,7 @@ ALL_CHECKS = [
     check_translation_invariance,
     check_permutation_equivariance,
     check_rows_and_threads,
+    check_rms_norm_mean_square,
+    check_rms_norm_vs_torch,
+    check_qk_norm_attention_vs_sdpa,
 ]

@@ -42,6 +42,20 @@ MUTANTS = {
                          "J->cos_t + 0 * (D / 2),\n                          J->sin_t + 0 * (D / 2)"),
     # values read from the key tensor
     "v_from_k": ("const double *vj = J->v +", "const double *vj = J->k +"),
+    # QK norm: eps added outside the square root
+    "norm_eps_outside": ("1.0 / sqrt(ss / (double)D + eps)", "1.0 / (sqrt(ss / (double)D) + eps)"),
+    # QK norm: sum of squares instead of their mean
+    "norm_sum_not_mean": ("sqrt(ss / (double)D + eps)", "sqrt(ss + eps)"),
+    # QK norm: learned weight ignored
+    "norm_no_weight": ("y[c] = x[c] * r * w[c];", "y[c] = x[c] * r;"),
+    # QK norm: text and image key weights swapped
+    "norm_segments_swapped": ("j < J->S_txt ? J->kw_txt : J->kw_img",
+                              "j < J->S_txt ? J->kw_img : J->kw_txt"),
+    # QK norm: keys normalised with the query weights
+    "norm_k_with_q_weights": ("j < J->S_txt ? J->kw_txt : J->kw_img",
+                              "j < J->S_txt ? J->qw_txt : J->qw_img"),
+    # QK norm: segment boundary off by one for the queries
+    "norm_segment_off_by_one": ("i < J->S_txt ? J->qw_txt", "i <= J->S_txt ? J->qw_txt"),
     # off-by-one in the key loop
     "skip_last_key": ("for (int64_t j = 0; j < S; ++j) {\n      double acc",
                       "for (int64_t j = 0; j < S - 1; ++j) {\n      double acc"),
