@@ -190,6 +190,10 @@ def run_ours(args, rank, world, local_rank):
     table = torch.empty((w.S, P), dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     krot = torch.empty(binding.krot_bytes(w.B, w.S, w.H, w.D), dtype=torch.uint8, device=dev)
+    qk_norm = None
+    if args.qk_norm:  # synthetic learned weights in [0.5, 1.5), one vector per stream and tensor
+        g = torch.Generator().manual_seed(7)
+        qk_norm = tuple((0.5 + torch.rand(w.D, generator=g)).to(dev) for _ in range(4)) + (1e-6,)
     stream = torch.cuda.Stream(device=dev)
 
     def step(i, ev_mid=None):
@@ -198,7 +202,7 @@ def run_ours(args, rank, world, local_rank):
         if ev_mid is not None:
             ev_mid.record(stream)
         binding.joint_rope_attention_tabled(q, k, v, table, status, out=out, stream=stream,
-                                            krot=krot)
+                                            krot=krot, qk_norm=qk_norm, s_txt=w.S_txt)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -268,6 +272,8 @@ def run_ours(args, rank, world, local_rank):
             "step": "rope_tables kernel + attention kernel (tables rebuilt every step)",
             "k_rope": "rotated K tiles shared by the CTAs of a head through an exchange "
                       f"buffer ({krot.numel() / 2**20:.0f} MiB)",
+            "qk_norm": ("fused QK RMS norm before RoPE (eps 1e-6, synthetic per-stream weights)"
+                        if args.qk_norm else "none"),
         },
         "pct_peak": round(100.0 * value / world / peak, 2),
         "roofline": {
@@ -431,6 +437,8 @@ def main():
     ap.add_argument("--workload", default="klein9b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--qk-norm", action="store_true",
+                    help="time the entry with the fused QK RMS normalisation before RoPE")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

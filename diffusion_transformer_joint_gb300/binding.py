@@ -25,6 +25,7 @@ STATUS = {
 EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_attention_workspace",
            "flux_joint_rope_attention_krot_bytes", "flux_joint_rope_attention_workspace_shared",
            "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
+           "flux_joint_qknorm_rope_attention", "flux_joint_qknorm_rope_attention_tabled",
            "flux_query_status", "flux_status_string")
 
 
@@ -71,6 +72,13 @@ def load(path: str | None = None):
             lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, I32, I64, I32, I32, V,
                                                              V, V, SZ, V]
             lib.flux_joint_rope_attention_tabled.restype = I32
+            F = ctypes.c_float
+            lib.flux_joint_qknorm_rope_attention.argtypes = [
+                V, V, V, V, I64, V, I64, I32, I32, I32, V, I32, D, V, V, V, V, F, V, V, SZ, V]
+            lib.flux_joint_qknorm_rope_attention.restype = I32
+            lib.flux_joint_qknorm_rope_attention_tabled.argtypes = [
+                V, V, V, V, I32, I64, I32, I32, I64, V, V, V, V, F, V, V, V, SZ, V]
+            lib.flux_joint_qknorm_rope_attention_tabled.restype = I32
             lib.flux_query_status.argtypes = [V, V]
             lib.flux_query_status.restype = I32
             lib.flux_status_string.argtypes = [I32]
@@ -172,14 +180,30 @@ def unpack_table(packed):
     return halves[..., 0].float(), halves[..., 1].float()
 
 
+def _norm_args(qk_norm, device):
+    """(q_txt, k_txt, q_img, k_img, eps) -> four fp32 CUDA [128] tensors and eps."""
+    import torch
+
+    *ws, eps = qk_norm
+    ts = []
+    for name, w in zip(("q_norm_txt", "k_norm_txt", "q_norm_img", "k_norm_img"), ws):
+        if not isinstance(w, torch.Tensor):
+            w = torch.as_tensor(w, dtype=torch.float32, device=device)
+        _need_cuda(name, w, torch.float32)
+        ts.append(w)
+    return ts, float(eps)
+
+
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA, out=None,
-                         workspace=None, stream=None, share_k=True):
+                         workspace=None, stream=None, share_k=True, qk_norm=None):
     """softmax(RoPE(q) RoPE(k)^T / sqrt(D)) v over the joint sequence [txt ; img].
 
     q, k, v: bf16 CUDA [B, S, H, 128]; txt_ids [S_txt, n_axes], img_ids
     [S_img, n_axes] int32 CUDA (either may be None / empty). Returns ``out``.
     Without ``workspace`` one is allocated: with room for the rotated-K
-    exchange buffer when ``share_k``, else the smallest one.
+    exchange buffer when ``share_k``, else the smallest one. ``qk_norm``:
+    None, or (q_norm_txt, k_norm_txt, q_norm_img, k_norm_img, eps) with fp32
+    [128] weights, for the QK RMS normalisation before RoPE.
     """
     import torch
 
@@ -202,19 +226,30 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
             n = workspace_bytes(max(S, 1), D)
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
     axes, n = _axes_array(axes_dims)
-    rc = lib.flux_joint_rope_attention(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes, n,
-        float(theta), _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if qk_norm is None:
+        rc = lib.flux_joint_rope_attention(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes,
+            n, float(theta), _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
+        name = "flux_joint_rope_attention"
+    else:
+        ws, eps = _norm_args(qk_norm, q.device)
+        rc = lib.flux_joint_qknorm_rope_attention(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes,
+            n, float(theta), *[_ptr(w) for w in ws], eps, _ptr(out), _ptr(workspace),
+            workspace.numel(), _stream_handle(stream))
+        name = "flux_joint_qknorm_rope_attention"
     if rc != 0:
-        raise FluxError("flux_joint_rope_attention", rc, lib)
+        raise FluxError(name, rc, lib)
     return out
 
 
-def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, krot=None):
+def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, krot=None,
+                                qk_norm=None, s_txt=0):
     """Attention with a caller-built packed table (see rope_tables_packed); ``status``
     is a device int32 tensor of one element that the caller clears. ``krot``: a
     uint8 CUDA tensor of at least krot_bytes(B, S, H) bytes serving as the
-    rotated-K exchange buffer; None allocates one, False runs without."""
+    rotated-K exchange buffer; None allocates one, False runs without.
+    ``qk_norm`` as for joint_rope_attention, with ``s_txt`` leading text tokens."""
     import torch
 
     lib = load()
@@ -232,11 +267,19 @@ def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, k
     else:
         _need_cuda("krot", krot, torch.uint8)
         kp, kn = _ptr(krot), krot.numel()
-    rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H, D,
-                                              _ptr(out), _ptr(status), kp, kn,
-                                              _stream_handle(stream))
+    if qk_norm is None:
+        rc = lib.flux_joint_rope_attention_tabled(_ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H,
+                                                  D, _ptr(out), _ptr(status), kp, kn,
+                                                  _stream_handle(stream))
+        name = "flux_joint_rope_attention_tabled"
+    else:
+        ws, eps = _norm_args(qk_norm, q.device)
+        rc = lib.flux_joint_qknorm_rope_attention_tabled(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H, D, int(s_txt),
+            *[_ptr(w) for w in ws], eps, _ptr(out), _ptr(status), kp, kn, _stream_handle(stream))
+        name = "flux_joint_qknorm_rope_attention_tabled"
     if rc != 0:
-        raise FluxError("flux_joint_rope_attention_tabled", rc, lib)
+        raise FluxError(name, rc, lib)
     return out
 
 

@@ -96,11 +96,25 @@ size_t flux_joint_rope_attention_workspace_shared(int B, int64_t S, int H, int D
   return (base == 0 || krot == 0) ? 0 : base + krot;
 }
 
-int flux_joint_rope_attention(const void *q, const void *k, const void *v,
-                              const int32_t *txt_ids, int64_t S_txt, const int32_t *img_ids,
-                              int64_t S_img, int B, int H, int D, const int32_t *axes_dims,
-                              int n_axes, double theta, void *out, void *workspace,
-                              size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// Checks of the QK-norm arguments: all four weight vectors or none; 16-byte
+// aligned fp32 [128]; eps finite and >= 0; S_txt within the sequence.
+int check_norm(const float *const w[4], float eps, int64_t S_txt, int64_t S) {
+  if (w[0] == nullptr || w[1] == nullptr || w[2] == nullptr || w[3] == nullptr)
+    return FLUX_ERR_NULL;
+  for (int i = 0; i < 4; ++i)
+    if (!aligned16(w[i])) return FLUX_ERR_ALIGN;
+  if (!(eps >= 0.f) || !(eps < 3.0e38f) || S_txt < 0 || S_txt > S) return FLUX_ERR_SHAPE;
+  return FLUX_OK;
+}
+
+int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
+             const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+             const int32_t *axes_dims, int n_axes, double theta, const float *const norm_w[4],
+             float eps, void *out, void *workspace, size_t workspace_bytes, void *stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
     return FLUX_ERR_NULL;
   if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr)) return FLUX_ERR_NULL;
@@ -113,6 +127,10 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
   const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
   if (rc != FLUX_OK) return rc;
   if (2 * pp.n_pairs != D) return FLUX_ERR_AXES;
+  if (norm_w != nullptr) {
+    const int nc = check_norm(norm_w, eps, S_txt, S);
+    if (nc != FLUX_OK) return nc;
+  }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FLUX_ERR_ALIGN;
   const size_t tensor_bytes = static_cast<size_t>(B) * static_cast<size_t>(S) *
                               static_cast<size_t>(H) * static_cast<size_t>(D) * 2;
@@ -123,7 +141,7 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < need)
     return FLUX_ERR_WORKSPACE;
-  // a workspace large enough for the rotated-K exchange buffer enables it
+  // a workspace large enough for the exchange buffer enables it
   const size_t need_shared = flux_joint_rope_attention_workspace_shared(B, S, H, D);
   const size_t used = (need_shared != 0 && workspace_bytes >= need_shared) ? need_shared : need;
   if (overlaps(workspace, used, q, tensor_bytes) || overlaps(workspace, used, k, tensor_bytes) ||
@@ -141,21 +159,27 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
                                nullptr, nullptr, table, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   void *krot = used == need ? nullptr : static_cast<void *>(ws + need);
-  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot, st) != cudaSuccess)
+  flux::QkNormArgs nargs{};
+  if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
+  if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot,
+                                   norm_w != nullptr ? &nargs : nullptr, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }
 
-int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
-                                     const uint32_t *table, int B, int64_t S, int H, int D,
-                                     void *out, int32_t *status, void *krot_scratch,
-                                     size_t krot_bytes, void *stream) {
+int tabled(const void *q, const void *k, const void *v, const uint32_t *table, int B, int64_t S,
+           int H, int D, int64_t S_txt, const float *const norm_w[4], float eps, void *out,
+           int32_t *status, void *krot_scratch, size_t krot_bytes, void *stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || table == nullptr ||
       status == nullptr)
     return FLUX_ERR_NULL;
   if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
     return FLUX_ERR_SHAPE;
   if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  if (norm_w != nullptr) {
+    const int nc = check_norm(norm_w, eps, S_txt, S);
+    if (nc != FLUX_OK) return nc;
+  }
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(table))
     return FLUX_ERR_ALIGN;
   const size_t tensor_bytes = static_cast<size_t>(B) * static_cast<size_t>(S) *
@@ -175,10 +199,59 @@ int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v
   }
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
+  flux::QkNormArgs nargs{};
+  if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot_scratch,
+                                   norm_w != nullptr ? &nargs : nullptr,
                                    static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int flux_joint_rope_attention(const void *q, const void *k, const void *v,
+                              const int32_t *txt_ids, int64_t S_txt, const int32_t *img_ids,
+                              int64_t S_img, int B, int H, int D, const int32_t *axes_dims,
+                              int n_axes, double theta, void *out, void *workspace,
+                              size_t workspace_bytes, void *stream) {
+  return one_call(q, k, v, txt_ids, S_txt, img_ids, S_img, B, H, D, axes_dims, n_axes, theta,
+                  nullptr, 0.f, out, workspace, workspace_bytes, stream);
+}
+
+int flux_joint_qknorm_rope_attention(const void *q, const void *k, const void *v,
+                                     const int32_t *txt_ids, int64_t S_txt,
+                                     const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                     const int32_t *axes_dims, int n_axes, double theta,
+                                     const float *q_norm_txt, const float *k_norm_txt,
+                                     const float *q_norm_img, const float *k_norm_img, float eps,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+  const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
+  return one_call(q, k, v, txt_ids, S_txt, img_ids, S_img, B, H, D, axes_dims, n_axes, theta, w,
+                  eps, out, workspace, workspace_bytes, stream);
+}
+
+int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
+                                     const uint32_t *table, int B, int64_t S, int H, int D,
+                                     void *out, int32_t *status, void *krot_scratch,
+                                     size_t krot_bytes, void *stream) {
+  return tabled(q, k, v, table, B, S, H, D, 0, nullptr, 0.f, out, status, krot_scratch,
+                krot_bytes, stream);
+}
+
+int flux_joint_qknorm_rope_attention_tabled(const void *q, const void *k, const void *v,
+                                            const uint32_t *table, int B, int64_t S, int H, int D,
+                                            int64_t S_txt, const float *q_norm_txt,
+                                            const float *k_norm_txt, const float *q_norm_img,
+                                            const float *k_norm_img, float eps, void *out,
+                                            int32_t *status, void *krot_scratch,
+                                            size_t krot_bytes, void *stream) {
+  const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
+  return tabled(q, k, v, table, B, S, H, D, S_txt, w, eps, out, status, krot_scratch, krot_bytes,
+                stream);
 }
 
 int flux_query_status(const void *workspace, void *stream) {

@@ -127,8 +127,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
 constexpr uint32_t kRegsSoftmax = 168;
-constexpr uint32_t kRegsCopyMma = 88;  // WG0: producers, MMA issuer
-constexpr uint32_t kRegsRope = 88;
+constexpr uint32_t kRegsCopyMma = 80;  // WG0: producers, MMA issuer
+constexpr uint32_t kRegsRope = 96;
 static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -151,6 +151,69 @@ __device__ __forceinline__ uint32_t rope_pair(uint32_t w, uint32_t cs) {
   return pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
 }
 
+// The same after scaling the two channels by s0 and s1 (the QK norm).
+__device__ __forceinline__ uint32_t rope_pair_scaled(uint32_t w, uint32_t cs, float s0, float s1) {
+  const float x0 = bf16lo_to_f32(w) * s0, x1 = bf16hi_to_f32(w) * s1;
+  const float c = f16lo_to_f32(cs), s = f16hi_to_f32(cs);
+  return pack_bf16x2(x0 * c - x1 * s, x0 * s + x1 * c);
+}
+
+// QK RMS normalisation applied before the rotation ("Diffusers 中
+// Flux2Transformer2DModel 全面解析", sections 内部架构双流块与单流块 and
+// 并行化支持: Q and K of each head are RMS-normalised over the head's 128
+// channels after their projections, text and image tokens with their own
+// learned weights; eps from 模型配置参数全解). For the tensor being rotated:
+// the weights of text tokens (token < s_txt) and of the others.
+struct QkNorm {
+  const float *w_txt, *w_img;
+  int64_t s_txt;
+  float eps;
+};
+
+// Per-channel scale of this thread's 8 channels (16-byte chunk c16) of a row
+// whose 8 bf16 values are `x`: the 16 lanes holding one row sum their squares
+// across shuffles, so all 32 lanes of the warp must call this together.
+__device__ __forceinline__ void qk_norm_scales(const uint4 &x, const QkNorm &nm, int64_t token,
+                                               int c16, float (&sc)[8]) {
+  const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float a = bf16lo_to_f32(wv[i]), b = bf16hi_to_f32(wv[i]);
+    ss = fmaf(a, a, ss);
+    ss = fmaf(b, b, ss);
+  }
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float r = rsqrtf(ss * (1.0f / kD) + nm.eps);
+  const float4 *w = reinterpret_cast<const float4 *>((token < nm.s_txt ? nm.w_txt : nm.w_img) + c16 * 8);
+  const float4 w0 = __ldg(w), w1 = __ldg(w + 1);
+  sc[0] = r * w0.x; sc[1] = r * w0.y; sc[2] = r * w0.z; sc[3] = r * w0.w;
+  sc[4] = r * w1.x; sc[5] = r * w1.y; sc[6] = r * w1.z; sc[7] = r * w1.w;
+}
+
+// Rotates the 8 channels of `x` with the (cos, sin) words `cs`, normalising
+// them first when kNorm.
+template <bool kNorm>
+__device__ __forceinline__ uint4 rope_chunk(const uint4 &x, const uint4 &cs, const QkNorm &nm,
+                                            int64_t token, int c16) {
+  uint4 o;
+  if (kNorm) {
+    float sc[8];
+    qk_norm_scales(x, nm, token, c16, sc);
+    o.x = rope_pair_scaled(x.x, cs.x, sc[0], sc[1]);
+    o.y = rope_pair_scaled(x.y, cs.y, sc[2], sc[3]);
+    o.z = rope_pair_scaled(x.z, cs.z, sc[4], sc[5]);
+    o.w = rope_pair_scaled(x.w, cs.w, sc[6], sc[7]);
+  } else {
+    o.x = rope_pair(x.x, cs.x);
+    o.y = rope_pair(x.y, cs.y);
+    o.z = rope_pair(x.z, cs.z);
+    o.w = rope_pair(x.w, cs.w);
+  }
+  return o;
+}
+
 // Hides a value's origin from the optimiser (no code is emitted).
 __device__ __forceinline__ void opaque(uint64_t &x) { asm volatile("" : "+l"(x)); }
 
@@ -168,31 +231,30 @@ __device__ __forceinline__ void reg_dec() {
 // ([64 rows][64 pairs] uint32; rows past the sequence end hold zeros, as do
 // the tile's). Thread u owns 16-byte column chunk u & 15 (channel pairs
 // 4(u&15) .. +3) of every 8th row. With kPublish the rotated rows below
-// rows_valid also go to global memory at grow + r * row_stride.
-template <bool kPublish = false>
+// rows_valid also go to global memory at grow + r * row_stride. With kNorm
+// the rows (token tok0 + r) are RMS-normalised first.
+template <bool kNorm, bool kPublish>
 __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int half, int u,
-                                            int rows_valid = 0, uint16_t *grow = nullptr,
-                                            int64_t row_stride = 0) {
+                                            const QkNorm &nm, int64_t tok0, int rows_valid,
+                                            uint16_t *grow, int64_t row_stride) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
-  // two batches of four rows: all loads of a batch in flight together
+  // batches of rows (four, or two with the norm's extra registers): all
+  // loads of a batch in flight together
+  constexpr int kBatch = kNorm ? 2 : 4;
 #pragma unroll
-  for (int i0 = 0; i0 < 8; i0 += 4) {
-    uint4 w[4], cs[4];
+  for (int i0 = 0; i0 < 8; i0 += kBatch) {
+    uint4 w[kBatch], cs[kBatch];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
       const int rh = (i0 + i) * 8 + rsub;
       w[i] = ld_shared_v4(tile + sw128_offset(half * 64 + rh, c16));
       cs[i] = ld_shared_v4(tbl + rh * (kPairs * 4) + c16 * 16);
     }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < kBatch; ++i) {
       const int r = half * 64 + (i0 + i) * 8 + rsub;
-      uint4 o;
-      o.x = rope_pair(w[i].x, cs[i].x);
-      o.y = rope_pair(w[i].y, cs[i].y);
-      o.z = rope_pair(w[i].z, cs[i].z);
-      o.w = rope_pair(w[i].w, cs[i].w);
+      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, c16);
       st_shared_v4(tile + sw128_offset(r, c16), o);
       if (kPublish && r < rows_valid) st_global_v4(grow + r * row_stride + c16 * 8, o);
     }
@@ -204,17 +266,23 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
 // row_stride elements apart, `tab` at the first row's packed table row. Thread
 // u owns 16-byte chunk u & 15 of rows (u >> 4) + 8 i, the row-to-thread map of
 // rotate_half, so RoPE warp w writes the rows r with r mod 8 in {2w, 2w+1}.
+// With kNorm the rows (token tok0 + r) are RMS-normalised first; every lane
+// of the warp runs every iteration (rows past nrows are zeros, not stored).
+template <bool kNorm>
 __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t *dst,
                                                    const uint32_t *tab, int nrows,
-                                                   int64_t row_stride, int u) {
+                                                   int64_t row_stride, int u, const QkNorm &nm,
+                                                   int64_t tok0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
 #pragma unroll 1
-  for (int i0 = 0; rsub + 8 * i0 < nrows; i0 += 2) {
+  for (int i0 = 0; (kNorm ? 8 * i0 : rsub + 8 * i0) < nrows; i0 += 2) {
     uint4 w[2], cs[2];
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int r = rsub + 8 * (i0 + i);
+      w[i] = make_uint4(0u, 0u, 0u, 0u);
+      cs[i] = make_uint4(0u, 0u, 0u, 0u);
       if (r < nrows) {
         w[i] = ld_global_nc_v4(src + r * row_stride + c16 * 8);
         cs[i] = ld_global_nc_v4(tab + static_cast<int64_t>(r) * kPairs + c16 * 4);
@@ -223,14 +291,8 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int r = rsub + 8 * (i0 + i);
-      if (r < nrows) {
-        uint4 o;
-        o.x = rope_pair(w[i].x, cs[i].x);
-        o.y = rope_pair(w[i].y, cs[i].y);
-        o.z = rope_pair(w[i].z, cs[i].z);
-        o.w = rope_pair(w[i].w, cs[i].w);
-        st_global_v4(dst + r * row_stride + c16 * 8, o);
-      }
+      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, c16);
+      if (r < nrows) st_global_v4(dst + r * row_stride + c16 * 8, o);
     }
   }
 }
@@ -267,13 +329,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// kNorm: Q and K are RMS-normalised (qn / kn) before the rotation.
+template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
-    joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ out,
-                                int *__restrict__ status, int64_t S, int H, int n_items,
-                                uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
-                                uint16_t *__restrict__ qrot, const uint16_t *__restrict__ qg,
-                                const uint16_t *__restrict__ kg,
-                                const uint32_t *__restrict__ tabg, uint64_t token) {
+    joint_rope_attention_kernel(const __grid_constant__ Maps maps, int *__restrict__ status,
+                                int64_t S, int H, int n_items, uint64_t *__restrict__ kflags,
+                                uint16_t *__restrict__ krot, uint16_t *__restrict__ qrot,
+                                const uint16_t *__restrict__ qg, const uint16_t *__restrict__ kg,
+                                const uint32_t *__restrict__ tabg, uint64_t token,
+                                const QkNorm qn, const QkNorm kn) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~static_cast<uintptr_t>(1023));
@@ -769,15 +833,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Rotates a landed tile whose first row is token tok0 in place; with
     // `grow` (K tiles when sharing) the rotated rows also go to the exchange
     // buffer. The table rows of its first half were requested already.
-    auto rotate_tile = [&](uint32_t tile, int64_t tok0, uint16_t *grow) {
+    auto rotate_tile = [&](uint32_t tile, int64_t tok0, uint16_t *grow, const QkNorm &nm) {
       const int rows_valid = static_cast<int>(S - tok0 < kBN ? (S - tok0 > 0 ? S - tok0 : 0) : kBN);
       for (int half = 0; ok && half < 2; ++half) {
         if (!(ok = mbar_wait_warp(bar(kBarTFull), static_cast<uint32_t>(tuse) & 1u, abort_flag)))
           return;
         if (grow != nullptr)
-          rotate_half<true>(tile, sbase + kOffT, half, u, rows_valid, grow, row_stride);
+          rotate_half<kNorm, true>(tile, sbase + kOffT, half, u, nm, tok0, rows_valid, grow,
+                                   row_stride);
         else
-          rotate_half(tile, sbase + kOffT, half, u);
+          rotate_half<kNorm, false>(tile, sbase + kOffT, half, u, nm, tok0, rows_valid, nullptr, 0);
         warp_arrive(bar(kBarTEmpty), lane);
         ++tuse;
         if (half == 0) load_table(tok0 + 64);
@@ -811,7 +876,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nrows = static_cast<int>(S - tok0 < 64 ? (S - tok0 > 0 ? S - tok0 : 0) : 64);
         const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
         if (nrows > 0)
-          rotate_rows_global(src + o, dst + o, tabg + tok0 * kPairs, nrows, row_stride, u);
+          rotate_rows_global<kNorm>(src + o, dst + o, tabg + tok0 * kPairs, nrows, row_stride, u,
+                                    c < 4 ? qn : kn, tok0);
         fence_proxy_async_global();  // read by TMA copies
         if (c >= 4 && ((c - 4) & 1) == 1) {
           // publish as the in-place path does: this warp's rows, then its flag
@@ -856,7 +922,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
         for (int t = 0; ok && t < kQTiles; ++t) {
           if (t > 0) load_table(static_cast<int64_t>(m0) + t * kBM);
-          rotate_tile(sbase + kOffQ + t * kTileBytes, static_cast<int64_t>(m0) + t * kBM, nullptr);
+          rotate_tile(sbase + kOffQ + t * kTileBytes, static_cast<int64_t>(m0) + t * kBM, nullptr,
+                      qn);
         }
         if (!ok) break;
         fence_proxy_async_smem();
@@ -873,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
       uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
-      rotate_tile(sbase + kOffK + s * kTileBytes, tok0, grow);
+      rotate_tile(sbase + kOffK + s * kTileBytes, tok0, grow, kn);
       if (!ok) break;
       fence_proxy_async_smem();
       if (share) {
@@ -980,7 +1047,8 @@ uint64_t next_launch_token() {
 
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
-                                   void *krot_scratch, cudaStream_t stream) {
+                                   void *krot_scratch, const QkNormArgs *norm,
+                                   cudaStream_t stream) {
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -988,9 +1056,13 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once[dev], [&] {
-    attr_err = cudaFuncSetAttribute(joint_rope_attention_kernel,
+    attr_err = cudaFuncSetAttribute(joint_rope_attention_kernel<false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     static_cast<int>(kSmemBytes));
+    if (attr_err == cudaSuccess)
+      attr_err = cudaFuncSetAttribute(joint_rope_attention_kernel<true>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(kSmemBytes));
   });
   if (attr_err != cudaSuccess) return attr_err;
   Maps maps;
@@ -1023,10 +1095,19 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   const int64_t items = static_cast<int64_t>(B) * H * ((S + kRowsPerCta - 1) / kRowsPerCta);
   if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
-  joint_rope_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(
-      maps, static_cast<uint16_t *>(out), status, S, H, static_cast<int>(items), kflags, krot, qrot,
-      static_cast<const uint16_t *>(q), static_cast<const uint16_t *>(k), table,
-      next_launch_token());
+  const uint16_t *qg = static_cast<const uint16_t *>(q), *kg = static_cast<const uint16_t *>(k);
+  if (norm != nullptr) {
+    const QkNorm qn{norm->q_txt, norm->q_img, norm->s_txt, norm->eps};
+    const QkNorm kn{norm->k_txt, norm->k_img, norm->s_txt, norm->eps};
+    joint_rope_attention_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(
+        maps, status, S, H, static_cast<int>(items), kflags, krot, qrot, qg, kg, table,
+        next_launch_token(), qn, kn);
+  } else {
+    const QkNorm none{nullptr, nullptr, 0, 0.f};
+    joint_rope_attention_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(
+        maps, status, S, H, static_cast<int>(items), kflags, krot, qrot, qg, kg, table,
+        next_launch_token(), none, none);
+  }
   return cudaGetLastError();
 }
 

@@ -62,13 +62,23 @@ inline size_t krot_scratch_bytes(int B, int64_t S, int H, int D) {
          2 * static_cast<size_t>(B) * static_cast<size_t>(S) * static_cast<size_t>(H) * 128 * 2;
 }
 
+// Optional QK RMS normalisation for launch_joint_attention: fp32 [128] device
+// weight vectors for the queries and keys of text tokens (the first s_txt
+// tokens) and of the other tokens, and eps.
+struct QkNormArgs {
+  const float *q_txt, *k_txt, *q_img, *k_img;
+  int64_t s_txt;
+  float eps;
+};
+
 // Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`
 // is the packed table of the joint sequence; status is the device status word.
 // `krot_scratch` (256-byte aligned, krot_scratch_bytes long) lets the CTAs
 // that work on one head share rotated K tiles; NULL makes every CTA rotate
-// every K tile it loads.
+// every K tile it loads. `norm` (nullable) normalises Q and K before RoPE.
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
-                                   void *krot_scratch, cudaStream_t stream);
+                                   void *krot_scratch, const QkNormArgs *norm,
+                                   cudaStream_t stream);
 
 }  // namespace flux

@@ -191,6 +191,46 @@ int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v
                                      void *out, int32_t *status, void *krot_scratch,
                                      size_t krot_bytes, void *stream);
 
+/*
+ * flux_joint_qknorm_rope_attention: flux_joint_rope_attention with the QK RMS
+ * normalisation that precedes RoPE in FLUX.2's attention ("Diffusers 中
+ * Flux2Transformer2DModel 全面解析", sections 内部架构双流块与单流块: Q and K
+ * are RMS-normalised right after their projections, text and image streams
+ * with their own weights; 并行化支持: over the whole head_dim; 模型配置参数全解:
+ * eps 1e-6). Every Q and K head vector x[D] becomes
+ *   x / sqrt(mean over the D channels of x^2 + eps) * w
+ * before the rotation, with w the text weights for the first S_txt tokens and
+ * the image weights for the others; V is not normalised.
+ *
+ *   q_norm_txt, k_norm_txt, q_norm_img, k_norm_img
+ *                device fp32 [D], 16-byte aligned (pass the same vectors for
+ *                both streams to use one weight set).
+ *   eps          finite, >= 0.
+ * Other arguments, layouts and return codes as flux_joint_rope_attention.
+ * Numerics: the norm and the rotation run in fp32 and round to bf16 once.
+ */
+int flux_joint_qknorm_rope_attention(const void *q, const void *k, const void *v,
+                                     const int32_t *txt_ids, int64_t S_txt,
+                                     const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                     const int32_t *axes_dims, int n_axes, double theta,
+                                     const float *q_norm_txt, const float *k_norm_txt,
+                                     const float *q_norm_img, const float *k_norm_img, float eps,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/*
+ * flux_joint_qknorm_rope_attention_tabled: flux_joint_rope_attention_tabled
+ * with the QK normalisation above; S_txt (0 .. S) is the number of leading
+ * text tokens, which use the text weights.
+ */
+int flux_joint_qknorm_rope_attention_tabled(const void *q, const void *k, const void *v,
+                                            const uint32_t *table, int B, int64_t S, int H, int D,
+                                            int64_t S_txt, const float *q_norm_txt,
+                                            const float *k_norm_txt, const float *q_norm_img,
+                                            const float *k_norm_img, float eps, void *out,
+                                            int32_t *status, void *krot_scratch,
+                                            size_t krot_bytes, void *stream);
+
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
  * on every device that loads this library, held until the process exits. */

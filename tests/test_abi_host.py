@@ -133,3 +133,30 @@ def test_tabled_exchange_buffer_checked_on_host(lib):
     assert _tabled(lib, 256 * 8192, need - 1) == -5        # too small
     assert _tabled(lib, 256, need) == -9                   # overlaps q
     assert _tabled(lib, 48 * 1024 * 1024 + 256, need) == -9  # overlaps out
+
+
+def test_qknorm_arguments_checked_on_host(lib):
+    P = ctypes.c_void_p
+    axes = (ctypes.c_int32 * 4)(32, 32, 32, 32)
+    W = 8 * 4096  # fake 16-byte-aligned weight vectors
+
+    def one_call(qt=W, kt=W + 512, qi=W + 1024, ki=W + 1536, eps=1e-6):
+        return lib.flux_joint_qknorm_rope_attention(
+            P(16), P(16 * 1024), P(32 * 1024), P(1024), 16, P(2048), 64, 1, 2, 128, axes, 4,
+            2000.0, P(qt) if qt else None, P(kt) if kt else None, P(qi) if qi else None,
+            P(ki) if ki else None, eps, P(48 * 1024 * 1024), P(256 * 4096), 1 << 20, None)
+
+    assert one_call(qt=0) == -1
+    assert one_call(ki=0) == -1
+    assert one_call(kt=W + 8) == -4
+    assert one_call(eps=-1.0) == -2
+    assert one_call(eps=float("nan")) == -2
+
+    def tab(s_txt):
+        return lib.flux_joint_qknorm_rope_attention_tabled(
+            P(16), P(16 * 1024), P(32 * 1024), P(4096 * 256), 1, 80, 2, 128, s_txt, P(W),
+            P(W + 512), P(W + 1024), P(W + 1536), 1e-6, P(48 * 1024 * 1024), P(64), None, 0,
+            None)
+
+    assert tab(81) == -2
+    assert tab(-1) == -2
