@@ -21,6 +21,9 @@ of V, and the attention agrees with torch's float64 SDPA and with a naive
 Python triple loop on tiny inputs. The optional QK RMS normalisation agrees
 with torch's float64 rms_norm and with its closed-form mean square, and the
 normalised attention with SDPA on inputs normalised and rotated separately.
+The reference KV modes agree with SDPA under an explicit boolean mask
+(extract) and over explicitly concatenated keys (cached), and a cache written
+in extract mode reproduces extract's text and image rows in cached mode.
 No function is "parity unpinned".
 """
 from __future__ import annotations
@@ -100,6 +103,14 @@ class Oracle:
             P, P, ctypes.c_int, ctypes.c_double, P, P, P, P, ctypes.c_int64, ctypes.c_double,
             P, ctypes.c_int64, ctypes.c_int, P]
         lib.oracle_joint_qknorm_rope_attention.restype = ctypes.c_int
+        lib.oracle_attention_extract.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int64, ctypes.c_int64, P, P, P]
+        lib.oracle_attention_extract.restype = ctypes.c_int
+        lib.oracle_attention_cached.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P]
+        lib.oracle_attention_cached.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -184,6 +195,51 @@ class Oracle:
         return out
 
 
+    def attention_extract(self, q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
+                          theta=2000.0):
+        """Extract mode over tokens [txt ; ref ; img]: (out [B, S, H, D], cache_k,
+        cache_v [B, S_ref, H, D]) in fp64."""
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        B, S, H, D = q.shape
+        axes = np.ascontiguousarray(axes_dims, dtype=np.int32)
+        n_t = 0 if txt_ids is None else np.asarray(txt_ids).reshape(-1, axes.size).shape[0]
+        n_r = 0 if ref_ids is None else np.asarray(ref_ids).reshape(-1, axes.size).shape[0]
+        ids = joint_ids(joint_ids(txt_ids, ref_ids) if n_t + n_r else None, img_ids)
+        assert ids.shape[0] == S
+        out = np.empty_like(q)
+        ck = np.empty((B, n_r, H, D))
+        cv = np.empty((B, n_r, H, D))
+        rc = self.lib.oracle_attention_extract(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids),
+                                               _ptr(axes), axes.size, float(theta), n_t, n_r,
+                                               _ptr(out), _ptr(ck), _ptr(cv))
+        if rc != 0:
+            raise ValueError("oracle_attention_extract: bad arguments")
+        return out, ck, cv
+
+    def attention_cached(self, q, k, v, txt_ids, img_ids, cache_k, cache_v,
+                         axes_dims=(32, 32, 32, 32), theta=2000.0):
+        """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; fp64 out."""
+        q = np.ascontiguousarray(q, dtype=np.float64)
+        k = np.ascontiguousarray(k, dtype=np.float64)
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        ck = np.ascontiguousarray(cache_k, dtype=np.float64)
+        cv = np.ascontiguousarray(cache_v, dtype=np.float64)
+        B, S, H, D = q.shape
+        axes = np.ascontiguousarray(axes_dims, dtype=np.int32)
+        n_t = 0 if txt_ids is None else np.asarray(txt_ids).reshape(-1, axes.size).shape[0]
+        ids = joint_ids(txt_ids, img_ids)
+        assert ids.shape[0] == S and ck.shape == cv.shape and ck.shape[0] == B
+        out = np.empty_like(q)
+        rc = self.lib.oracle_attention_cached(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids),
+                                              _ptr(axes), axes.size, float(theta), n_t, _ptr(ck),
+                                              _ptr(cv), ck.shape[1], _ptr(out))
+        if rc != 0:
+            raise ValueError("oracle_attention_cached: bad arguments")
+        return out
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -202,6 +258,17 @@ def rope_apply(x, cos_t, sin_t):
 
 def rms_norm(x, w, eps=1e-6):
     return default().rms_norm(x, w, eps)
+
+
+def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
+                      theta=2000.0):
+    return default().attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims, theta)
+
+
+def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=(32, 32, 32, 32),
+                     theta=2000.0):
+    return default().attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims,
+                                      theta)
 
 
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),

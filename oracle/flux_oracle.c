@@ -42,6 +42,15 @@
  *      text tokens (the first S_txt) with the text weights, the others with
  *      the image weights; V is not normalised.
  *
+ *   5. Reference-image KV modes ("Diffusers 中 Flux2Transformer2DModel 全面解析",
+ *      section "参考图 KV 缓存机制": the cache holds the reference tokens' K
+ *      after RoPE and their V, [B, n_ref, H, D]; in "extract" mode the
+ *      sequence is [txt, ref, img], reference queries attend to reference
+ *      keys only while text and image queries attend to every token, and the
+ *      reference K / V are stored to the cache; in "cached" mode the sequence
+ *      is [txt, img] and the cached reference K / V are inserted between the
+ *      text and the image keys and values).
+ *
  * Layout: q, k, v, out are [B, S, H, D] row-major (D fastest), in double.
  * ids are [S, n_axes] int32 and are shared by every batch element.
  */
@@ -276,4 +285,146 @@ int oracle_joint_qknorm_rope_attention(
   return joint_attention(q, k, v, B, S, H, D, ids, axes_dims, n_axes, theta, qw_txt,
                          kw_txt, qw_img, kw_img, S_txt, eps, rows, n_rows, n_threads,
                          out);
+}
+
+/* ---- reference KV modes, step 5 --------------------------------------- */
+
+/* Softmax-weighted sum over keys [k_lo, k_hi) of rotated keys khat (rows of
+ * D) and values vrow(j) for one rotated query qhat. */
+static void attend_range(const double *qhat, const double *khat, const double *const *vrows,
+                         int64_t k_lo, int64_t k_hi, int D, double *z, double *o) {
+  const double scale = 1.0 / sqrt((double)D);
+  double zmax = -INFINITY;
+  for (int64_t j = k_lo; j < k_hi; ++j) {
+    double acc = 0.0;
+    for (int c = 0; c < D; ++c) acc += qhat[c] * khat[j * D + c];
+    z[j] = scale * acc;
+    if (z[j] > zmax) zmax = z[j];
+  }
+  double denom = 0.0;
+  for (int64_t j = k_lo; j < k_hi; ++j) {
+    z[j] = exp(z[j] - zmax);
+    denom += z[j];
+  }
+  for (int c = 0; c < D; ++c) o[c] = 0.0;
+  for (int64_t j = k_lo; j < k_hi; ++j) {
+    const double wj = z[j] / denom;
+    for (int c = 0; c < D; ++c) o[c] += wj * vrows[j][c];
+  }
+}
+
+/* Extract mode. Tokens [txt ; ref ; img] (S_txt, S_ref, then the rest), ids
+ * [S, n_axes] in the same order. out [B, S, H, D]: reference queries attend
+ * to the reference keys, every other query to all S keys. cache_k / cache_v
+ * [B, S_ref, H, D]: the reference tokens' rotated K and their V. Single
+ * threaded. Returns 0, or -1 on bad arguments. */
+int oracle_attention_extract(const double *q, const double *k, const double *v, int B,
+                             int64_t S, int H, int D, const int32_t *ids,
+                             const int32_t *axes_dims, int n_axes, double theta,
+                             int64_t S_txt, int64_t S_ref, double *out, double *cache_k,
+                             double *cache_v) {
+  int sum = 0;
+  for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
+  if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0 || S_txt < 0 || S_ref < 0 ||
+      S_txt + S_ref > S)
+    return -1;
+  double *cos_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  double *sin_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  if (oracle_rope_tables(ids, S, axes_dims, n_axes, theta, cos_t, sin_t) != 0) {
+    free(cos_t);
+    free(sin_t);
+    return -1;
+  }
+  double *khat = (double *)malloc(sizeof(double) * (size_t)S * D);
+  double *qhat = (double *)malloc(sizeof(double) * (size_t)D);
+  double *z = (double *)malloc(sizeof(double) * (size_t)S);
+  const double **vrows = (const double **)malloc(sizeof(double *) * (size_t)S);
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      for (int64_t j = 0; j < S; ++j) {
+        const int64_t off = (((int64_t)b * S + j) * H + h) * D;
+        oracle_rope_apply_vec(k + off, cos_t + j * (D / 2), sin_t + j * (D / 2), D,
+                              khat + j * D);
+        vrows[j] = v + off;
+      }
+      for (int64_t i = 0; i < S; ++i) {
+        const int64_t off = (((int64_t)b * S + i) * H + h) * D;
+        oracle_rope_apply_vec(q + off, cos_t + i * (D / 2), sin_t + i * (D / 2), D, qhat);
+        const int is_ref = i >= S_txt && i < S_txt + S_ref;
+        attend_range(qhat, khat, vrows, is_ref ? S_txt : 0, is_ref ? S_txt + S_ref : S, D, z,
+                     out + off);
+      }
+      for (int64_t r = 0; r < S_ref; ++r) {
+        const int64_t coff = (((int64_t)b * S_ref + r) * H + h) * D;
+        for (int c = 0; c < D; ++c) {
+          cache_k[coff + c] = khat[(S_txt + r) * D + c];
+          cache_v[coff + c] = vrows[S_txt + r][c];
+        }
+      }
+    }
+  free(khat);
+  free(qhat);
+  free(z);
+  free(vrows);
+  free(cos_t);
+  free(sin_t);
+  return 0;
+}
+
+/* Cached mode. Queries, keys and values of the tokens [txt ; img] (S_txt,
+ * then the rest; ids [S, n_axes] in that order) and a cache [B, S_ref, H, D]
+ * of reference keys (already rotated) and values. Every query attends to the
+ * keys [txt ; cached ref ; img]. out [B, S, H, D]. Single threaded. Returns
+ * 0, or -1 on bad arguments. */
+int oracle_attention_cached(const double *q, const double *k, const double *v, int B,
+                            int64_t S, int H, int D, const int32_t *ids,
+                            const int32_t *axes_dims, int n_axes, double theta, int64_t S_txt,
+                            const double *cache_k, const double *cache_v, int64_t S_ref,
+                            double *out) {
+  int sum = 0;
+  for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
+  if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0 || S_txt < 0 || S_txt > S ||
+      S_ref < 0)
+    return -1;
+  const int64_t Sk = S + S_ref;
+  double *cos_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  double *sin_t = (double *)malloc(sizeof(double) * (size_t)S * (D / 2));
+  if (oracle_rope_tables(ids, S, axes_dims, n_axes, theta, cos_t, sin_t) != 0) {
+    free(cos_t);
+    free(sin_t);
+    return -1;
+  }
+  double *khat = (double *)malloc(sizeof(double) * (size_t)Sk * D);
+  double *qhat = (double *)malloc(sizeof(double) * (size_t)D);
+  double *z = (double *)malloc(sizeof(double) * (size_t)Sk);
+  const double **vrows = (const double **)malloc(sizeof(double *) * (size_t)Sk);
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      /* keys in the order [txt ; cached ref ; img] */
+      for (int64_t j = 0; j < Sk; ++j) {
+        if (j >= S_txt && j < S_txt + S_ref) {
+          const int64_t coff = (((int64_t)b * S_ref + (j - S_txt)) * H + h) * D;
+          for (int c = 0; c < D; ++c) khat[j * D + c] = cache_k[coff + c];
+          vrows[j] = cache_v + coff;
+        } else {
+          const int64_t t = j < S_txt ? j : j - S_ref; /* token of [txt ; img] */
+          const int64_t off = (((int64_t)b * S + t) * H + h) * D;
+          oracle_rope_apply_vec(k + off, cos_t + t * (D / 2), sin_t + t * (D / 2), D,
+                                khat + j * D);
+          vrows[j] = v + off;
+        }
+      }
+      for (int64_t i = 0; i < S; ++i) {
+        const int64_t off = (((int64_t)b * S + i) * H + h) * D;
+        oracle_rope_apply_vec(q + off, cos_t + i * (D / 2), sin_t + i * (D / 2), D, qhat);
+        attend_range(qhat, khat, vrows, 0, Sk, D, z, out + off);
+      }
+    }
+  free(khat);
+  free(qhat);
+  free(z);
+  free(vrows);
+  free(cos_t);
+  free(sin_t);
+  return 0;
 }

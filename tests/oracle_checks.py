@@ -331,6 +331,73 @@ def check_qk_norm_attention_vs_sdpa(orc):
     assert np.allclose(out2, out3, rtol=0, atol=1e-12)
 
 
+# ---------------------------------------------------- reference KV modes
+
+
+def _sdpa_masked_f64(qh, kh, v, mask):
+    """torch float64 SDPA with a boolean mask [S_q, S_k] (True = attend)."""
+    import torch
+
+    q_t = torch.from_numpy(qh).permute(0, 2, 1, 3)
+    k_t = torch.from_numpy(kh).permute(0, 2, 1, 3)
+    v_t = torch.from_numpy(v).permute(0, 2, 1, 3)
+    o = torch.nn.functional.scaled_dot_product_attention(q_t, k_t, v_t,
+                                                         attn_mask=torch.from_numpy(mask))
+    return o.permute(0, 2, 1, 3).contiguous().numpy()
+
+
+def check_extract_mode_vs_masked_sdpa(orc):
+    """[txt ; ref ; img]: reference queries see reference keys only, the rest
+    see every key (a boolean mask for torch's SDPA); the cache holds the
+    reference keys rotated (complex exponentials) and their values."""
+    rng = _rng(19)
+    B, n_t, n_r, n_i, H, D = 2, 5, 11, 14, 2, 128
+    S = n_t + n_r + n_i
+    txt, ref, img = _rand_ids(rng, n_t), _rand_ids(rng, n_r), _rand_ids(rng, n_i)
+    ids = np.concatenate([txt, ref, img])
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    out, ck, cv = orc.attention_extract(q, k, v, txt, ref, img)
+    mask = np.ones((S, S), dtype=bool)
+    mask[n_t:n_t + n_r, :] = False
+    mask[n_t:n_t + n_r, n_t:n_t + n_r] = True
+    kh = _rotate_all(k, ids, FLUX_AXES, FLUX_THETA)
+    ref_out = _sdpa_masked_f64(_rotate_all(q, ids, FLUX_AXES, FLUX_THETA), kh, v, mask)
+    assert np.allclose(out, ref_out, rtol=0, atol=1e-11), np.abs(out - ref_out).max()
+    assert np.allclose(ck, kh[:, n_t:n_t + n_r], rtol=0, atol=1e-12)
+    assert np.array_equal(cv, v[:, n_t:n_t + n_r])
+
+
+def check_cached_mode_vs_concatenated_sdpa(orc):
+    """[txt ; img] queries over keys [txt ; cache ; img] built explicitly."""
+    rng = _rng(20)
+    B, n_t, n_i, n_r, H, D = 1, 6, 21, 9, 3, 128
+    S = n_t + n_i
+    txt, img = _rand_ids(rng, n_t), _rand_ids(rng, n_i)
+    ids = np.concatenate([txt, img])
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    ck, cv = rng.standard_normal((B, n_r, H, D)), rng.standard_normal((B, n_r, H, D))
+    out = orc.attention_cached(q, k, v, txt, img, ck, cv)
+    kh = _rotate_all(k, ids, FLUX_AXES, FLUX_THETA)
+    keys = np.concatenate([kh[:, :n_t], ck, kh[:, n_t:]], axis=1)
+    vals = np.concatenate([v[:, :n_t], cv, v[:, n_t:]], axis=1)
+    ref_out = _sdpa_f64(_rotate_all(q, ids, FLUX_AXES, FLUX_THETA), keys, vals)
+    assert np.allclose(out, ref_out, rtol=0, atol=1e-11), np.abs(out - ref_out).max()
+
+
+def check_extract_then_cached_reproduces_rows(orc):
+    """The cache's purpose: with the same text and image inputs, cached mode
+    gives the text and image rows that extract mode gave."""
+    rng = _rng(21)
+    B, n_t, n_r, n_i, H, D = 1, 4, 10, 17, 2, 128
+    txt, ref, img = _rand_ids(rng, n_t), _rand_ids(rng, n_r), _rand_ids(rng, n_i)
+    S = n_t + n_r + n_i
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    out, ck, cv = orc.attention_extract(q, k, v, txt, ref, img)
+    keep = np.r_[0:n_t, n_t + n_r:S]
+    out2 = orc.attention_cached(q[:, keep], k[:, keep], v[:, keep], txt, img, ck, cv)
+    assert np.allclose(out2, out[:, keep], rtol=0, atol=1e-12)
+
+
 ALL_CHECKS = [
     check_zero_ids_identity,
     check_frequencies_high_precision,
@@ -349,4 +416,7 @@ ALL_CHECKS = [
     check_rms_norm_mean_square,
     check_rms_norm_vs_torch,
     check_qk_norm_attention_vs_sdpa,
+    check_extract_mode_vs_masked_sdpa,
+    check_cached_mode_vs_concatenated_sdpa,
+    check_extract_then_cached_reproduces_rows,
 ]

@@ -56,6 +56,25 @@ MUTANTS = {
                               "j < J->S_txt ? J->qw_txt : J->qw_img"),
     # QK norm: segment boundary off by one for the queries
     "norm_segment_off_by_one": ("i < J->S_txt ? J->qw_txt", "i <= J->S_txt ? J->qw_txt"),
+    # KV modes: no 1/sqrt(D) scale
+    "range_no_scale": ("z[j] = scale * acc;", "z[j] = acc;"),
+    # KV modes: softmax not normalised
+    "range_no_normalise": ("const double wj = z[j] / denom;", "const double wj = z[j];"),
+    # extract: reference queries attend to every key
+    "extract_ref_sees_all": ("is_ref ? S_txt : 0, is_ref ? S_txt + S_ref : S",
+                             "0, S"),
+    # extract: text and image queries restricted to the reference keys too
+    "extract_all_restricted": ("is_ref ? S_txt : 0, is_ref ? S_txt + S_ref : S",
+                               "S_txt, S_txt + S_ref"),
+    # extract: the cache holds the unrotated keys
+    "extract_cache_unrotated": ("cache_k[coff + c] = khat[(S_txt + r) * D + c];",
+                                "cache_k[coff + c] = k[(((int64_t)b * S + S_txt + r) * H + h) * D + c];"),
+    # cached: the cached keys rotated again by the query-side table
+    "cached_rerotated": ("for (int c = 0; c < D; ++c) khat[j * D + c] = cache_k[coff + c];",
+                         "oracle_rope_apply_vec(cache_k + coff, cos_t, sin_t, D, khat + j * D);"),
+    # cached: image keys read from the wrong token (offset by the cache length)
+    "cached_img_offset": ("const int64_t t = j < S_txt ? j : j - S_ref;",
+                          "const int64_t t = j < S_txt ? j : (j - S_ref + 1) % S;"),
     # off-by-one in the key loop
     "skip_last_key": ("for (int64_t j = 0; j < S; ++j) {\n      double acc",
                       "for (int64_t j = 0; j < S - 1; ++j) {\n      double acc"),
