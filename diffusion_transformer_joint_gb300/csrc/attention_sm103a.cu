@@ -127,8 +127,8 @@ static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 // Register split (setmaxnreg): 512 threads x 128 registers at launch.
 constexpr uint32_t kRegsSoftmax = 168;
-constexpr uint32_t kRegsCopyMma = 80;  // WG0: producers, MMA issuer
-constexpr uint32_t kRegsRope = 96;
+constexpr uint32_t kRegsCopyMma = 72;  // WG0: producers, MMA issuer
+constexpr uint32_t kRegsRope = 104;
 static_assert(128 * (2 * kRegsSoftmax + kRegsCopyMma + kRegsRope) == 512 * 128,
               "warpgroup register shares must add up to the launch allocation");
 
@@ -298,7 +298,30 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
 }
 
 struct Maps {
-  CUtensorMap q, k, v, out, krot, qrot, table;
+  CUtensorMap q, k, v, out, krot, qrot, table_q, table_k;
+};
+
+// A work item: batch b, head h, the 256 query rows from m0 (rows of Q / out
+// at or past q_hi belong to another segment: computed, never stored), its key
+// range [k_lo, k_hi) of K / V in n_tiles 128-key tiles walked from tile j0,
+// and the publication flags of that key range for (b, h) ([n_tiles][4]; null
+// without the exchange buffer).
+struct Item {
+  int b, h, n_tiles, j0;
+  int64_t m0, q_hi, k_lo, k_hi;
+  uint64_t *flags;
+};
+
+// The segments of one launch, by value: segment g owns items
+// [first_item[g], first_item[g + 1]), queries [q_lo, q_hi) in n_rb 256-row
+// blocks and keys [k_lo, k_hi) in n_tiles tiles; flag_off is the word offset
+// of its key range's flags in the exchange buffer.
+struct Segs {
+  int n;
+  int first_item[kMaxSegments + 1];
+  int n_rb[kMaxSegments], n_tiles[kMaxSegments];
+  int64_t q_lo[kMaxSegments], q_hi[kMaxSegments], k_lo[kMaxSegments], k_hi[kMaxSegments];
+  int64_t flag_off[kMaxSegments];
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -332,11 +355,14 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
 // kNorm: Q and K are RMS-normalised (qn / kn) before the rotation.
 template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
-    joint_rope_attention_kernel(const __grid_constant__ Maps maps, int *__restrict__ status,
-                                int64_t S, int H, int n_items, uint64_t *__restrict__ kflags,
-                                uint16_t *__restrict__ krot, uint16_t *__restrict__ qrot,
-                                const uint16_t *__restrict__ qg, const uint16_t *__restrict__ kg,
-                                const uint32_t *__restrict__ tabg, uint64_t token,
+    joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ outg,
+                                int *__restrict__ status,
+                                const Segs sg, int64_t S_q, int64_t S_k, int H, int n_items,
+                                uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
+                                uint16_t *__restrict__ qrot, const uint16_t *__restrict__ qg,
+                                const uint16_t *__restrict__ kg,
+                                const uint32_t *__restrict__ tabq,
+                                const uint32_t *__restrict__ tabk, uint64_t token,
                                 const QkNorm qn, const QkNorm kn) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -351,25 +377,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const int64_t row_stride = static_cast<int64_t>(H) * kD;
-  const int n_tiles = static_cast<int>((S + kBN - 1) / kBN);
-  const int n_rb = static_cast<int>((S + kRowsPerCta - 1) / kRowsPerCta);  // row blocks per head
-  // Work items (batch, head, row block), row block fastest, handed out round
-  // robin: CTAs running at the same time share the K/V of a few heads in L2.
-  auto decode = [&](int item, int &b, int &h, int &m0) {
-    m0 = (item % n_rb) * kRowsPerCta;
-    const int bh = item / n_rb;
-    h = bh % H;
-    b = bh / H;
-  };
-  // Key tiles are walked starting at a tile that depends on the row block,
-  // spread evenly over the head: the CTAs working on one head at the same
-  // time each rotate different K tiles first and publish them (kflags /
-  // krot), so that later each mostly loads tiles another CTA rotated.
-  auto first_tile = [&](int m0) {
-    return static_cast<int>((static_cast<int64_t>(m0 / kRowsPerCta) * n_tiles) / n_rb);
-  };
-  auto tile_at = [&](int j0, int j) { return j0 + j < n_tiles ? j0 + j : j0 + j - n_tiles; };
   const bool share = kflags != nullptr;
+  // Work items: segment by segment, (batch, head, 256-row block) with the row
+  // block fastest, handed out round robin, so CTAs running at the same time
+  // share the K/V of a few heads in L2. Key tiles are walked from a start
+  // tile that depends on the row block, spread evenly over the key range:
+  // the CTAs working on one head at the same time each rotate different K
+  // tiles first and publish them (kflags / krot), and later each mostly
+  // loads tiles another CTA rotated.
+  auto info = [&](int item) {
+    Item it;
+    int g = 0;
+    while (g + 1 < sg.n && item >= sg.first_item[g + 1]) ++g;
+    const int local = item - sg.first_item[g];
+    const int nrb = sg.n_rb[g];
+    const int rb = local % nrb;
+    const int bh = local / nrb;
+    it.h = bh % H;
+    it.b = bh / H;
+    it.m0 = sg.q_lo[g] + static_cast<int64_t>(rb) * kRowsPerCta;
+    it.q_hi = sg.q_hi[g];
+    it.k_lo = sg.k_lo[g];
+    it.k_hi = sg.k_hi[g];
+    it.n_tiles = sg.n_tiles[g];
+    it.j0 = static_cast<int>((static_cast<int64_t>(rb) * it.n_tiles) / nrb);
+    it.flags = share ? kflags + sg.flag_off[g] +
+                           (static_cast<int64_t>(it.b) * H + it.h) * it.n_tiles * 4
+                     : nullptr;
+    return it;
+  };
+  auto tile_at = [&](const Item &it, int j) {
+    return it.j0 + j < it.n_tiles ? it.j0 + j : it.j0 + j - it.n_tiles;
+  };
+  // first key row of tile tj of the item's key range
+  auto tile_row = [&](const Item &it, int tj) { return it.k_lo + static_cast<int64_t>(tj) * kBN; };
 
   if (tid == 0) {
     mbar_init(bar(kBarQRaw), 1);
@@ -446,8 +487,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // parity of the phase it completes
       uint32_t last_k_full = 0, last_k_par = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
-        int b, h, m0;
-        decode(item, b, h, m0);
+        const Item it = info(item);
+        const int b = it.b, h = it.h, m0 = static_cast<int>(it.m0);
         const int next = item + static_cast<int>(gridDim.x);
         // the previous item's S MMAs no longer read the Q buffers
         if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
@@ -480,10 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           post(kRqQ | (last_q_parity << 8), static_cast<uint32_t>(item));
           ++q_local;
         }
-        const int j0 = first_tile(m0);
+        const int n_tiles = it.n_tiles;
         const int prep_at = n_tiles > kPrepAtTile ? kPrepAtTile : n_tiles - 1;
-        const uint64_t *fl_head =
-            share ? kflags + (static_cast<int64_t>(b) * H + h) * n_tiles * 4 : nullptr;
         int pieces = 0;  // prepare pieces posted for the next item, one per key tile
         for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
           while (share && next < n_items && pieces < kPrepChunks &&
@@ -493,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           const int s = jt % kStages;
-          const int tj = tile_at(j0, j);
+          const int tj = tile_at(it, j);
+          const int krow = static_cast<int>(tile_row(it, tj));
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           // Has every RoPE warp of some CTA published tile tj? Decided (and
           // the acquire fence paid) before the ring wait, which hides both.
@@ -501,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // RoPE warps, ordered before this point by the Q-prep wait.
           bool rotated = share && k > 0 && j < 2;
           if (share && !rotated) {
-            const uint64_t *fl = fl_head + static_cast<int64_t>(tj) * 4;
+            const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
             ld_relaxed_gpu_v2_u64(fl, f0, f1);
             ld_relaxed_gpu_v2_u64(fl + 2, f2, f3);
@@ -519,8 +559,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_k_full |= 1u << s;
             last_k_par = (last_k_par & ~(1u << s)) | ((use & 1u) << s);
             mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-            tma_load_4d(dst, &maps.krot, bar(kBarKFull + s), 0, h, tj * kBN, b);
-            tma_load_4d(dst + kBlockBytes, &maps.krot, bar(kBarKFull + s), 64, h, tj * kBN, b);
+            tma_load_4d(dst, &maps.krot, bar(kBarKFull + s), 0, h, krow, b);
+            tma_load_4d(dst + kBlockBytes, &maps.krot, bar(kBarKFull + s), 64, h, krow, b);
             mbar_arrive_n(bar(kBarKFull + s), 3);
           } else {
             const uint32_t par = (raw_par >> s) & 1u;
@@ -528,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_k_full &= ~(1u << s);
             last_k_par = (last_k_par & ~(1u << s)) | (par << s);
             mbar_arrive_expect_tx(bar(kBarKRaw + s), kTileBytes);
-            tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, tj * kBN, b);
-            tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, tj * kBN, b);
+            tma_load_4d(dst, &maps.k, bar(kBarKRaw + s), 0, h, krow, b);
+            tma_load_4d(dst + kBlockBytes, &maps.k, bar(kBarKRaw + s), 64, h, krow, b);
             post(kRqK | (static_cast<uint32_t>(s) << 4) | (par << 8) |
                      (static_cast<uint32_t>(tj) << 9),
                  static_cast<uint32_t>(item));
@@ -538,11 +578,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the exchange buffer the RoPE warps have read it long before)
           if (!share && j == (n_tiles > kQPrefetchTiles ? n_tiles - kQPrefetchTiles : 0) &&
               next < n_items) {
-            int nb, nh, nm0;
-            decode(next, nb, nh, nm0);
-            for (int t = 0; t < kQTiles && nm0 + t * kBM < S; ++t) {
-              tma_prefetch_l2_4d(&maps.q, 0, nh, nm0 + t * kBM, nb);
-              tma_prefetch_l2_4d(&maps.q, 64, nh, nm0 + t * kBM, nb);
+            const Item nx = info(next);
+            const int nm0 = static_cast<int>(nx.m0);
+            for (int t = 0; t < kQTiles && nm0 + t * kBM < S_q; ++t) {
+              tma_prefetch_l2_4d(&maps.q, 0, nx.h, nm0 + t * kBM, nx.b);
+              tma_prefetch_l2_4d(&maps.q, 64, nx.h, nm0 + t * kBM, nx.b);
             }
           }
         }
@@ -563,24 +603,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       int jt = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        int b, h, m0;
-        decode(item, b, h, m0);
-        const int j0 = first_tile(m0);
+        const Item it = info(item);
+        const int b = it.b, h = it.h, n_tiles = it.n_tiles;
         for (int j = 0; j < n_tiles; ++j, ++jt) {
           const int s = jt % kStages;
-          const int tj = tile_at(j0, j);
+          const int vrow = static_cast<int>(tile_row(it, tile_at(it, j)));
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           const uint32_t dst = sbase + kOffV + s * kTileBytes;
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, tj * kBN, b);
-          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, tj * kBN, b);
+          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, vrow, b);
+          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, vrow, b);
           // the tile two ahead into L2 now, so that its copy does not wait on
           // DRAM when the ring frees up
           if (j + kVPrefetch < n_tiles) {
-            const int tp = tile_at(j0, j + kVPrefetch);
-            tma_prefetch_l2_4d(&maps.v, 0, h, tp * kBN, b);
-            tma_prefetch_l2_4d(&maps.v, 64, h, tp * kBN, b);
+            const int prow = static_cast<int>(tile_row(it, tile_at(it, j + kVPrefetch)));
+            tma_prefetch_l2_4d(&maps.v, 0, h, prow, b);
+            tma_prefetch_l2_4d(&maps.v, 64, h, prow, b);
           }
         }
       }
@@ -613,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int k = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
+        const int n_tiles = info(item).n_tiles;
         if (!(ok = mbar_wait_warp(bar(kBarQFull), static_cast<uint32_t>(k) & 1u, abort_flag))) break;
         {
           const int s0 = jt % kStages;
@@ -686,9 +726,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int jt = 0;
     for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      int b, h, m0;
-      decode(item, b, h, m0);
-      const int j0 = first_tile(m0);
+      const Item it = info(item);
+      const int b = it.b, h = it.h, n_tiles = it.n_tiles;
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < n_tiles; ++j, ++jt) {
         if (!(ok = mbar_wait_warp(bar(kBarSFull + t), static_cast<uint32_t>(jt) & 1u, abort_flag))) break;
@@ -699,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN / 32; ++c)
           tmem_ld32_max(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]), mr[c]);
         tmem_ld_wait();
-        const int valid = static_cast<int>(S - static_cast<int64_t>(tile_at(j0, j)) * kBN);
+        const int64_t kv = it.k_hi - tile_row(it, tile_at(it, j));  // keys of this tile in range
+        const int valid = static_cast<int>(kv < kBN ? kv : kBN);
         float mx = fmax3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
         if (valid < kBN) {
 #pragma unroll
@@ -776,10 +816,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       // Each warp stages its 32 rows, 32 channels at a time, in its own
       // 64-byte-swizzled 2 KB buffer and lane 0 stores them with one TMA copy
-      // (rows past the sequence end are not written).
+      // (rows past the tensor's end are not written). A box that would cross
+      // the end of the item's query segment inside the tensor is written row
+      // by row instead, rows of the next segment left alone.
       const float inv_l = 1.f / l_run;
       const uint32_t stage = sbase + kOffStage + static_cast<uint32_t>(warp - 4) * kStageWarpBytes;
-      const int row0 = m0 + t * kBM + wq * 32;
+      const int64_t row0 = it.m0 + t * kBM + wq * 32;
+      const bool box_ok = row0 < it.q_hi && (row0 + 32 <= it.q_hi || it.q_hi == S_q);
+      const bool row_ok = row0 + lane < it.q_hi;
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t o[32];
@@ -795,12 +839,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
           w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
           w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-          st_shared_v4(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
+          if (box_ok)
+            st_shared_v4(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
+          else if (row_ok)
+            st_global_v4(outg + ((static_cast<int64_t>(b) * S_q + row0 + lane) * H + h) * kD +
+                             c * 32 + q * 8,
+                         w);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && row0 < S) {
-          tma_store_4d(&maps.out, stage, c * 32, h, row0, b);
+        if (lane == 0 && box_ok) {
+          tma_store_4d(&maps.out, stage, c * 32, h, static_cast<int>(row0), b);
           bulk_commit();
         }
       }
@@ -815,26 +864,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     int tuse = 0;   // table-buffer halves consumed so far
     int tload = 0;  // table-buffer loads issued (RoPE warp 0)
-    // Table rows [row0, row0 + 64) into the shared buffer: RoPE warp 0 loads
-    // them once every RoPE warp is done with the previous rows.
-    auto load_table = [&](int64_t row0) {
+    // Table rows [row0, row0 + 64) of the Q-side or K-side table into the
+    // shared buffer: RoPE warp 0 loads them once every RoPE warp is done with
+    // the previous rows.
+    auto load_table = [&](const CUtensorMap *tmap, int64_t row0) {
       if (u < 32) {
         if (!(ok = mbar_wait_warp(bar(kBarTEmpty), (static_cast<uint32_t>(tuse) & 1u) ^ 1u,
                                   abort_flag)))
           return;
         if (lane == 0) {
           mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
-          tma_load_2d(sbase + kOffT, &maps.table, bar(kBarTFull), 0, static_cast<int>(row0));
+          tma_load_2d(sbase + kOffT, tmap, bar(kBarTFull), 0, static_cast<int>(row0));
         }
         __syncwarp();
         ++tload;
       }
     };
-    // Rotates a landed tile whose first row is token tok0 in place; with
-    // `grow` (K tiles when sharing) the rotated rows also go to the exchange
-    // buffer. The table rows of its first half were requested already.
-    auto rotate_tile = [&](uint32_t tile, int64_t tok0, uint16_t *grow, const QkNorm &nm) {
-      const int rows_valid = static_cast<int>(S - tok0 < kBN ? (S - tok0 > 0 ? S - tok0 : 0) : kBN);
+    // Rotates a landed tile whose first row is row tok0 of a tensor of
+    // n_rows rows in place; with `grow` (K tiles when sharing) the rotated
+    // rows also go to the exchange buffer. The table rows of its first half
+    // were requested already.
+    auto rotate_tile = [&](uint32_t tile, int64_t tok0, int64_t n_rows, uint16_t *grow,
+                           const QkNorm &nm, const CUtensorMap *tmap) {
+      const int rows_valid =
+          static_cast<int>(n_rows - tok0 < kBN ? (n_rows - tok0 > 0 ? n_rows - tok0 : 0) : kBN);
       for (int half = 0; ok && half < 2; ++half) {
         if (!(ok = mbar_wait_warp(bar(kBarTFull), static_cast<uint32_t>(tuse) & 1u, abort_flag)))
           return;
@@ -845,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           rotate_half<kNorm, false>(tile, sbase + kOffT, half, u, nm, tok0, rows_valid, nullptr, 0);
         warp_arrive(bar(kBarTEmpty), lane);
         ++tuse;
-        if (half == 0) load_table(tok0 + 64);
+        if (half == 0) load_table(tmap, tok0 + 64);
       }
     };
     // Prepares piece c of the CTA's next item while the current one runs:
@@ -857,37 +910,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     // the two K tiles without reading flags. Small pieces keep raw K tiles
     // from waiting long behind this work.
     auto prepare_piece = [&](int next, int c) {
-      int nb, nh, nm0;
-      decode(next, nb, nh, nm0);
+      const Item nx = info(next);
       const int kt = (c - 4) >> 1;  // K tile (0 or 1) of pieces 4-7
-      if (c < 4 || kt < n_tiles) {
-        int64_t tok0;
+      if (c < 4 || kt < nx.n_tiles) {
+        int64_t tok0, n_rows;
         const uint16_t *src;
         uint16_t *dst;
+        const uint32_t *tab;
         if (c < 4) {
-          tok0 = static_cast<int64_t>(nm0) + c * 64;
-          src = qg;
-          dst = qrot;
+          tok0 = nx.m0 + c * 64;
+          n_rows = S_q;
+          src = qg + ((static_cast<int64_t>(nx.b) * S_q + tok0) * H + nx.h) * kD;
+          dst = qrot + ((static_cast<int64_t>(nx.b) * S_q + tok0) * H + nx.h) * kD;
+          tab = tabq;
         } else {
-          tok0 = static_cast<int64_t>(tile_at(first_tile(nm0), kt)) * kBN + ((c - 4) & 1) * 64;
-          src = kg;
-          dst = krot;
+          tok0 = tile_row(nx, tile_at(nx, kt)) + ((c - 4) & 1) * 64;
+          n_rows = S_k;
+          src = kg + ((static_cast<int64_t>(nx.b) * S_k + tok0) * H + nx.h) * kD;
+          dst = krot + ((static_cast<int64_t>(nx.b) * S_k + tok0) * H + nx.h) * kD;
+          tab = tabk;
         }
-        const int nrows = static_cast<int>(S - tok0 < 64 ? (S - tok0 > 0 ? S - tok0 : 0) : 64);
-        const int64_t o = ((static_cast<int64_t>(nb) * S + tok0) * H + nh) * kD;
+        const int nrows = static_cast<int>(n_rows - tok0 < 64 ? (n_rows - tok0 > 0 ? n_rows - tok0 : 0) : 64);
         if (nrows > 0)
-          rotate_rows_global<kNorm>(src + o, dst + o, tabg + tok0 * kPairs, nrows, row_stride, u,
+          rotate_rows_global<kNorm>(src, dst, tab + tok0 * kPairs, nrows, row_stride, u,
                                     c < 4 ? qn : kn, tok0);
         fence_proxy_async_global();  // read by TMA copies
         if (c >= 4 && ((c - 4) & 1) == 1) {
           // publish as the in-place path does: this warp's rows, then its flag
-          const int tj = tile_at(first_tile(nm0), kt);
           fence_acq_rel_gpu();
           __syncwarp();
           if (lane == 0) {
             fence_acq_rel_gpu();
-            st_relaxed_gpu_u64(
-                kflags + ((static_cast<int64_t>(nb) * H + nh) * n_tiles + tj) * 4 + (u >> 5), token);
+            st_relaxed_gpu_u64(nx.flags + static_cast<int64_t>(tile_at(nx, kt)) * 4 + (u >> 5),
+                               token);
           }
         }
       }
@@ -914,16 +969,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const uint32_t par = (x >> 8) & 1u;
+      const Item it = info(item);
       if (kind == kRqQ) {
-        int b, h, m0;
-        decode(item, b, h, m0);
-        load_table(m0);
+        load_table(&maps.table_q, it.m0);
         if (!ok) break;
         if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
         for (int t = 0; ok && t < kQTiles; ++t) {
-          if (t > 0) load_table(static_cast<int64_t>(m0) + t * kBM);
-          rotate_tile(sbase + kOffQ + t * kTileBytes, static_cast<int64_t>(m0) + t * kBM, nullptr,
-                      qn);
+          if (t > 0) load_table(&maps.table_q, it.m0 + t * kBM);
+          rotate_tile(sbase + kOffQ + t * kTileBytes, it.m0 + t * kBM, S_q, nullptr, qn,
+                      &maps.table_q);
         }
         if (!ok) break;
         fence_proxy_async_smem();
@@ -933,14 +987,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       // kind == kRqK: a raw K tile in stage s
       const int s = static_cast<int>((x >> 4) & 15u);
       const int tj = static_cast<int>(x >> 9);
-      int b, h, m0;
-      decode(item, b, h, m0);
-      const int64_t tok0 = static_cast<int64_t>(tj) * kBN;
-      load_table(tok0);  // in flight while the tile itself lands
+      const int64_t tok0 = tile_row(it, tj);
+      load_table(&maps.table_k, tok0);  // in flight while the tile itself lands
       if (!ok) break;
       if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
-      uint16_t *grow = share ? krot + ((static_cast<int64_t>(b) * S + tok0) * H + h) * kD : nullptr;
-      rotate_tile(sbase + kOffK + s * kTileBytes, tok0, grow, kn);
+      uint16_t *grow =
+          share ? krot + ((static_cast<int64_t>(it.b) * S_k + tok0) * H + it.h) * kD : nullptr;
+      rotate_tile(sbase + kOffK + s * kTileBytes, tok0, S_k, grow, kn, &maps.table_k);
       if (!ok) break;
       fence_proxy_async_smem();
       if (share) {
@@ -951,8 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) {
           fence_acq_rel_gpu();
-          st_relaxed_gpu_u64(
-              kflags + ((static_cast<int64_t>(b) * H + h) * n_tiles + tj) * 4 + (u >> 5), token);
+          st_relaxed_gpu_u64(it.flags + static_cast<int64_t>(tj) * 4 + (u >> 5), token);
         }
       }
       warp_arrive(bar(kBarKFull + s), lane);
@@ -1045,10 +1097,26 @@ uint64_t next_launch_token() {
   return z == 0 ? 1 : z;
 }
 
-cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
-                                   const uint32_t *table, int *status, int B, int64_t S, int H,
-                                   void *krot_scratch, const QkNormArgs *norm,
-                                   cudaStream_t stream) {
+size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment *segs,
+                      int n_segs) {
+  size_t flags = 0;
+  for (int r = 0; r < kMaxSegments; ++r)
+    for (int g = 0; g < n_segs; ++g)
+      if (segs[g].key_range == r) {  // the first segment of each key range sizes its flags
+        flags += static_cast<size_t>(B) * H * ((segs[g].k_hi - segs[g].k_lo + kBN - 1) / kBN) * 4;
+        break;
+      }
+  flags = (flags * sizeof(uint64_t) + 255) & ~static_cast<size_t>(255);
+  return flags + (static_cast<size_t>(B) * static_cast<size_t>(S_k) * H * kD +
+                  static_cast<size_t>(B) * static_cast<size_t>(S_q) * H * kD) * 2;
+}
+
+cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
+                                      const uint32_t *table_q, const uint32_t *table_k,
+                                      int *status, int B, int64_t S_q, int64_t S_k, int H,
+                                      const AttnSegment *segs, int n_segs, void *xbuf,
+                                      const QkNormArgs *norm, cudaStream_t stream) {
+  if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1066,19 +1134,51 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
   });
   if (attr_err != cudaSuccess) return attr_err;
   Maps maps;
-  if (!make_head_map(&maps.q, q, B, S, H) || !make_head_map(&maps.k, k, B, S, H) ||
-      !make_head_map(&maps.v, v, B, S, H) || !make_head_map(&maps.out, out, B, S, H, 32, 32) ||
-      !make_table_map(&maps.table, table, S))
+  if (!make_head_map(&maps.q, q, B, S_q, H) || !make_head_map(&maps.k, k, B, S_k, H) ||
+      !make_head_map(&maps.v, v, B, S_k, H) || !make_head_map(&maps.out, out, B, S_q, H, 32, 32) ||
+      !make_table_map(&maps.table_q, table_q, S_q) || !make_table_map(&maps.table_k, table_k, S_k))
     return cudaErrorInvalidValue;
+  // segments, their items and their key ranges' flag offsets
+  Segs sg{};
+  sg.n = n_segs;
+  int64_t items = 0;
+  int64_t range_off[kMaxSegments];
+  int64_t off = 0;
+  for (int r = 0; r < kMaxSegments; ++r) {
+    range_off[r] = -1;
+    for (int g = 0; g < n_segs; ++g)
+      if (segs[g].key_range == r) {
+        range_off[r] = off;
+        off += static_cast<int64_t>(B) * H * ((segs[g].k_hi - segs[g].k_lo + kBN - 1) / kBN) * 4;
+        break;
+      }
+  }
+  for (int g = 0; g < n_segs; ++g) {
+    const AttnSegment &a = segs[g];
+    if (a.q_lo < 0 || a.q_hi > S_q || a.k_lo < 0 || a.k_hi > S_k || a.k_hi <= a.k_lo ||
+        a.key_range < 0 || a.key_range >= kMaxSegments)
+      return cudaErrorInvalidValue;
+    sg.first_item[g] = static_cast<int>(items);
+    sg.q_lo[g] = a.q_lo;
+    sg.q_hi[g] = a.q_hi;
+    sg.k_lo[g] = a.k_lo;
+    sg.k_hi[g] = a.k_hi;
+    sg.n_rb[g] = static_cast<int>((a.q_hi - a.q_lo + kRowsPerCta - 1) / kRowsPerCta);
+    sg.n_tiles[g] = static_cast<int>((a.k_hi - a.k_lo + kBN - 1) / kBN);
+    sg.flag_off[g] = range_off[a.key_range];
+    items += static_cast<int64_t>(B) * H * (a.q_hi > a.q_lo ? sg.n_rb[g] : 0);
+    if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  }
+  sg.first_item[n_segs] = static_cast<int>(items);
+  if (items == 0) return cudaSuccess;
   uint64_t *kflags = nullptr;
   uint16_t *krot = nullptr, *qrot = nullptr;
-  if (krot_scratch != nullptr) {
-    const size_t tensor = static_cast<size_t>(B) * static_cast<size_t>(S) * H * kD * 2;
-    kflags = static_cast<uint64_t *>(krot_scratch);
-    krot = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(krot_scratch) +
-                                        krot_flag_bytes(B, S, H));
-    qrot = reinterpret_cast<uint16_t *>(reinterpret_cast<uint8_t *>(krot) + tensor);
-    if (!make_head_map(&maps.krot, krot, B, S, H) || !make_head_map(&maps.qrot, qrot, B, S, H))
+  if (xbuf != nullptr) {
+    const size_t flags = (static_cast<size_t>(off) * sizeof(uint64_t) + 255) & ~static_cast<size_t>(255);
+    kflags = static_cast<uint64_t *>(xbuf);
+    krot = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(xbuf) + flags);
+    qrot = krot + static_cast<size_t>(B) * static_cast<size_t>(S_k) * H * kD;
+    if (!make_head_map(&maps.krot, krot, B, S_k, H) || !make_head_map(&maps.qrot, qrot, B, S_q, H))
       return cudaErrorInvalidValue;
   } else {
     maps.krot = maps.k;  // never read
@@ -1092,23 +1192,31 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
     if (e != cudaSuccess) return e;
     sm_count[dev] = n;
   }
-  const int64_t items = static_cast<int64_t>(B) * H * ((S + kRowsPerCta - 1) / kRowsPerCta);
-  if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
   const uint16_t *qg = static_cast<const uint16_t *>(q), *kg = static_cast<const uint16_t *>(k);
+  uint16_t *og = static_cast<uint16_t *>(out);
   if (norm != nullptr) {
     const QkNorm qn{norm->q_txt, norm->q_img, norm->s_txt, norm->eps};
     const QkNorm kn{norm->k_txt, norm->k_img, norm->s_txt, norm->eps};
     joint_rope_attention_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(
-        maps, status, S, H, static_cast<int>(items), kflags, krot, qrot, qg, kg, table,
-        next_launch_token(), qn, kn);
+        maps, og, status, sg, S_q, S_k, H, static_cast<int>(items), kflags, krot, qrot, qg, kg,
+        table_q, table_k, next_launch_token(), qn, kn);
   } else {
     const QkNorm none{nullptr, nullptr, 0, 0.f};
     joint_rope_attention_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(
-        maps, status, S, H, static_cast<int>(items), kflags, krot, qrot, qg, kg, table,
-        next_launch_token(), none, none);
+        maps, og, status, sg, S_q, S_k, H, static_cast<int>(items), kflags, krot, qrot, qg, kg,
+        table_q, table_k, next_launch_token(), none, none);
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
+                                   const uint32_t *table, int *status, int B, int64_t S, int H,
+                                   void *krot_scratch, const QkNormArgs *norm,
+                                   cudaStream_t stream) {
+  const AttnSegment all{0, S, 0, S, 0};
+  return launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, &all, 1,
+                                   krot_scratch, norm, stream);
 }
 
 }  // namespace flux

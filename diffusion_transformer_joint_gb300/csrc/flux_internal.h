@@ -71,6 +71,32 @@ struct QkNormArgs {
   float eps;
 };
 
+// One segment of a launch: queries [q_lo, q_hi) (rows of Q / out) attend to
+// keys [k_lo, k_hi) (rows of K / V). Segments with the same key_range
+// (0 .. kMaxSegments-1) must have the same key range and share its
+// exchange-buffer flags.
+constexpr int kMaxSegments = 3;
+struct AttnSegment {
+  int64_t q_lo, q_hi, k_lo, k_hi;
+  int key_range;
+};
+
+// Bytes of the exchange buffer of launch_attention_segments: the flags of
+// each key range, padded to 256 bytes, then bf16 [B, S_k, H, D] rotated K
+// and [B, S_q, H, D] rotated Q.
+size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment *segs,
+                      int n_segs);
+
+// Enqueues the attention kernel over segments: Q / out [B, S_q, H, 128] and
+// K / V [B, S_k, H, 128] bf16; table_q [S_q, 64] and table_k [S_k, 64]
+// packed tables for the rows of Q and of K; xbuf (nullable) the exchange
+// buffer of exchange_bytes(...) bytes, 256-byte aligned.
+cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
+                                      const uint32_t *table_q, const uint32_t *table_k,
+                                      int *status, int B, int64_t S_q, int64_t S_k, int H,
+                                      const AttnSegment *segs, int n_segs, void *xbuf,
+                                      const QkNormArgs *norm, cudaStream_t stream);
+
 // Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`
 // is the packed table of the joint sequence; status is the device status word.
 // `krot_scratch` (256-byte aligned, krot_scratch_bytes long) lets the CTAs
