@@ -6,12 +6,16 @@ Q/K tile loads, QK^T and PV on tcgen05, online softmax). FLOPs per step are
 4 * B * H * S^2 * 128.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload klein9b]
+                    [--workload klein9b] [--qk-norm] [--kv-mode extract|cached]
 
 Prints one JSON line (rank 0). With N > 1 (torchrun, one rank per GPU) every
 rank runs the same-shaped workload on its own seeded inputs with no data
 exchange (heads and batches are independent): weak scaling, and `value` is
 all ranks' FLOPs over the slowest rank's time.
+
+`--kv-mode extract|cached` times one reference-image KV-mode call per step on
+the two-reference edit shape instead (tables, attention and the cache copies
+or key/value gathers inside the call).
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload.
@@ -343,6 +347,203 @@ def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
     return {"ms_per_step": e0.elapsed_time(e1) / K, "h2d": h2d, "d2h": d2h}
 
 
+# --------------------------------------------------------- reference-image KV modes
+
+
+def kv_split(w):
+    """An edit workload as the KV pipeline orders it, [txt ; refs ; img]:
+    (S_txt, S_ref, S_img)."""
+    S_i = w.grid * w.grid
+    return w.S_txt, w.S_img - S_i, S_i
+
+
+def kv_flops(w, mode):
+    """Extract: text and image queries against all S keys, reference queries
+    against the reference keys. Cached: text and image queries against
+    [txt ; cache ; img]. 4 flops per (query, key, channel)."""
+    S_t, S_r, S_i = kv_split(w)
+    per = 4 * w.B * w.H * w.D
+    if mode == "extract":
+        return per * ((S_t + S_i) * w.S + S_r * S_r)
+    return per * (S_t + S_i) * w.S
+
+
+def _kv_host_inputs(w, mode, seed_offset, W, np):
+    """bf16 CPU tensors and int32 ids of one KV-mode call (refs moved before img)."""
+    S_t, S_r, S_i = kv_split(w)
+    q, k, v = W.workload_qkv(w, seed_offset=seed_offset)  # [txt ; img ; refs]
+    t_ids, i_ids = W.workload_ids(w)
+    ids = np.concatenate([t_ids, i_ids])
+    if mode == "extract":
+        order = np.r_[0:S_t, S_t + S_i:w.S, S_t:S_t + S_i]
+        q, k, v = (x[:, order].contiguous() for x in (q, k, v))
+        ids = ids[order]
+        return (q, k, v), (ids[:S_t], ids[S_t:S_t + S_r], ids[S_t + S_r:])
+    keep = np.r_[0:S_t + S_i]
+    q, k, v = (x[:, keep].contiguous() for x in (q, k, v))
+    ck = W.normal_bf16((w.B, S_r, w.H, w.D), 1000 * w.index + seed_offset + 7)
+    cv = W.normal_bf16((w.B, S_r, w.H, w.D), 1000 * w.index + seed_offset + 8)
+    return (q, k, v, ck, cv), (ids[:S_t], ids[S_t:S_t + S_i])
+
+
+def run_kv(args, rank, world, local_rank):
+    """Time one KV-mode call per step (ids -> tables -> attention -> cache)."""
+    import numpy as np
+    import torch
+
+    from diffusion_transformer_joint_gb300 import binding
+    from diffusion_transformer_joint_gb300 import build as cuda_build
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(cuda_build.LIB_PATH):
+        cuda_build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+    w = W.WORKLOADS[args.workload]
+    mode = args.kv_mode
+    S_t, S_r, S_i = kv_split(w)
+    if S_r == 0:
+        raise SystemExit(f"--kv-mode needs a workload with reference images, not {w.name}")
+
+    def to_dev(xs):
+        return tuple(torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+                     if isinstance(x, np.ndarray) else x.to(dev) for x in xs)
+
+    tensors0, ids_h = _kv_host_inputs(w, mode, rank_seed_offset(rank, 0), W, np)
+    set_bytes = sum(t.numel() * 2 for t in tensors0)
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    ids = to_dev(ids_h)
+    sets = []
+    for i in range(n_sets):
+        ts = tensors0 if i == 0 else _kv_host_inputs(w, mode, rank_seed_offset(rank, i), W, np)[0]
+        ts = to_dev(ts)
+        outs = (torch.empty_like(ts[0]),)
+        if mode == "extract":
+            outs += tuple(torch.empty((w.B, S_r, w.H, w.D), dtype=torch.bfloat16, device=dev)
+                          for _ in range(2))
+        sets.append((ts, outs))
+    n_ws = (binding.extract_workspace_bytes(w.B, S_t, S_r, S_i, w.H, w.D) if mode == "extract"
+            else binding.cached_workspace_bytes(w.B, S_t, S_i, S_r, w.H, w.D))
+    ws = torch.zeros(int(n_ws), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def call(ts, outs, st):
+        if mode == "extract":
+            binding.attention_extract(*ts, *ids, out=outs[0], cache_k=outs[1], cache_v=outs[2],
+                                      workspace=ws, stream=st)
+        else:
+            q, k, v, ck, cv = ts
+            binding.attention_cached(q, k, v, ids[0], ids[1], ck, cv, out=outs[0], workspace=ws,
+                                     stream=st)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            call(*sets[i % n_sets], stream)
+    stream.synchronize()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(K):
+                call(*sets[i % n_sets], stream)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    if binding.query_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    t_max = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+
+    # end to end: pinned host inputs in, the call, the outputs (and cache) back
+    h_in = tuple(t.pin_memory() for t in tensors0)
+    h_ids = tuple(torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in ids_h)
+    d_in = tuple(torch.empty_like(t, device=dev) for t in h_in)
+    d_ids = tuple(torch.empty_like(t, device=dev) for t in h_ids)
+    d_out = sets[0][1]
+    h_out = tuple(torch.empty_like(t, device="cpu").pin_memory() for t in d_out)
+
+    def e2e_one():
+        for d, h in zip(d_in + d_ids, h_in + h_ids):
+            d.copy_(h, non_blocking=True)
+        if mode == "extract":
+            binding.attention_extract(*d_in, *d_ids, out=d_out[0], cache_k=d_out[1],
+                                      cache_v=d_out[2], workspace=ws, stream=stream)
+        else:
+            q, k, v, ck, cv = d_in
+            binding.attention_cached(q, k, v, d_ids[0], d_ids[1], ck, cv, out=d_out[0],
+                                     workspace=ws, stream=stream)
+        for h, d in zip(h_out, d_out):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_one()
+        e1.record(stream)
+    stream.synchronize()
+    if binding.query_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
+    if rank != 0:
+        return None
+
+    peaks, peak_src = _peaks()
+    flops = kv_flops(w, mode)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    call_ms = t_max / K
+    value = whole_job_tflops(flops, world, K, t_max)
+    per_call = flops / (call_ms * 1e-3) / 1e12
+    keys = "[txt ; refs ; img]" if mode == "extract" else "[txt ; cache ; img]"
+    queries = "all S (refs against refs only)" if mode == "extract" else f"{S_t + S_i} (txt ; img)"
+    return {
+        "metric": f"{mode}-mode joint RoPE-attention bf16 TFLOP/s at the klein-9B two-reference "
+                  "edit shape",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(call_ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v and cache, FLUX.2 (T,H,W,L) ids)",
+        "config": {
+            "workload": f"{w.name} {mode}: B={w.B} H={w.H} text {S_t}, refs {S_r}, image {S_i}; "
+                        f"queries {queries}, keys {keys}; head_dim={w.D} theta=2000",
+            "B": w.B, "H": w.H, "S_txt": S_t, "S_ref": S_r, "S_img": S_i, "head_dim": w.D,
+            "parallelism": f"replicas x{world} (no collective)",
+            "l2": f"inputs rotate over {n_sets} sets of {set_bytes / 2**20:.0f} MiB "
+                  f"({n_sets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
+            "step": ("two table kernels, the attention kernel over 3 segments, two cache copies"
+                     if mode == "extract" else
+                     "two table kernels, two key/value gathers, the attention kernel"),
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "whole call (tables + attention + copies)",
+            "achieved": round(per_call, 2), "peak": peak, "unit": "TFLOP/s",
+            "frac": round(per_call / peak, 4),
+            "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+        },
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(whole_job_tflops(flops, world, 1, e2e_ms), 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in + h_ids),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
+                "api": f"flux_joint_rope_attention_{mode}"},
+        "gpu_launches": 3 * K,
+    }
+
+
 # --------------------------------------------------------- CPU baseline
 
 
@@ -437,6 +638,8 @@ def main():
     ap.add_argument("--workload", default="klein9b")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kv-mode", choices=("extract", "cached"), default=None,
+                    help="time a reference-image KV-mode call on an edit workload instead")
     ap.add_argument("--qk-norm", action="store_true",
                     help="time the entry with the fused QK RMS normalisation before RoPE")
     args = ap.parse_args()
@@ -455,7 +658,12 @@ def main():
 
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl")
-        line = run_ours(args, rank, world, local_rank)
+        if args.kv_mode is not None:
+            if args.workload == "klein9b":
+                args.workload = "klein9b_edit2"
+            line = run_kv(args, rank, world, local_rank)
+        else:
+            line = run_ours(args, rank, world, local_rank)
         if world > 1:
             import torch.distributed as dist
 

@@ -26,6 +26,8 @@ EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_atten
            "flux_joint_rope_attention_krot_bytes", "flux_joint_rope_attention_workspace_shared",
            "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
            "flux_joint_qknorm_rope_attention", "flux_joint_qknorm_rope_attention_tabled",
+           "flux_joint_rope_attention_extract_workspace", "flux_joint_rope_attention_extract",
+           "flux_joint_rope_attention_cached_workspace", "flux_joint_rope_attention_cached",
            "flux_query_status", "flux_status_string")
 
 
@@ -79,6 +81,16 @@ def load(path: str | None = None):
             lib.flux_joint_qknorm_rope_attention_tabled.argtypes = [
                 V, V, V, V, I32, I64, I32, I32, I64, V, V, V, V, F, V, V, V, SZ, V]
             lib.flux_joint_qknorm_rope_attention_tabled.restype = I32
+            lib.flux_joint_rope_attention_extract_workspace.argtypes = [I32, I64, I64, I64, I32, I32]
+            lib.flux_joint_rope_attention_extract_workspace.restype = SZ
+            lib.flux_joint_rope_attention_extract.argtypes = [
+                V, V, V, V, I64, V, I64, V, I64, I32, I32, I32, V, I32, D, V, V, V, V, SZ, V]
+            lib.flux_joint_rope_attention_extract.restype = I32
+            lib.flux_joint_rope_attention_cached_workspace.argtypes = [I32, I64, I64, I64, I32, I32]
+            lib.flux_joint_rope_attention_cached_workspace.restype = SZ
+            lib.flux_joint_rope_attention_cached.argtypes = [
+                V, V, V, V, I64, V, I64, V, V, I64, I32, I32, I32, V, I32, D, V, V, SZ, V]
+            lib.flux_joint_rope_attention_cached.restype = I32
             lib.flux_query_status.argtypes = [V, V]
             lib.flux_query_status.restype = I32
             lib.flux_status_string.argtypes = [I32]
@@ -126,6 +138,20 @@ def krot_bytes(B: int, S: int, H: int, D: int = 128) -> int:
 def workspace_shared_bytes(B: int, S: int, H: int, D: int = 128) -> int:
     """Workspace size with which joint_rope_attention shares rotated K tiles."""
     return int(load().flux_joint_rope_attention_workspace_shared(int(B), int(S), int(H), int(D)))
+
+
+def extract_workspace_bytes(B: int, S_txt: int, S_ref: int, S_img: int, H: int,
+                            D: int = 128) -> int:
+    """Workspace size of one attention_extract call (0: bad shape)."""
+    return int(load().flux_joint_rope_attention_extract_workspace(int(B), int(S_txt), int(S_ref),
+                                                                 int(S_img), int(H), int(D)))
+
+
+def cached_workspace_bytes(B: int, S_txt: int, S_img: int, S_ref: int, H: int,
+                           D: int = 128) -> int:
+    """Workspace size of one attention_cached call (0: bad shape)."""
+    return int(load().flux_joint_rope_attention_cached_workspace(int(B), int(S_txt), int(S_img),
+                                                                int(S_ref), int(H), int(D)))
 
 
 def rope_tables(ids, axes_dims=AXES_DIMS, theta=THETA, cos_out=None, sin_out=None, stream=None):
@@ -280,6 +306,68 @@ def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, k
         name = "flux_joint_qknorm_rope_attention_tabled"
     if rc != 0:
         raise FluxError(name, rc, lib)
+    return out
+
+
+def _rows(ids):
+    return 0 if ids is None else int(ids.shape[0])
+
+
+def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA,
+                      out=None, cache_k=None, cache_v=None, workspace=None, stream=None):
+    """Extract mode over tokens [txt ; ref ; img]: returns (out, cache_k, cache_v)."""
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+    B, S, H, D = q.shape
+    s_t, s_r, s_i = _rows(txt_ids), _rows(ref_ids), _rows(img_ids)
+    for name, t in (("txt_ids", txt_ids), ("ref_ids", ref_ids), ("img_ids", img_ids)):
+        if t is not None and t.numel() > 0:
+            _need_cuda(name, t, torch.int32)
+    out = torch.empty_like(q) if out is None else out
+    if cache_k is None:
+        cache_k = torch.empty((B, s_r, H, D), dtype=torch.bfloat16, device=q.device)
+    if cache_v is None:
+        cache_v = torch.empty((B, s_r, H, D), dtype=torch.bfloat16, device=q.device)
+    if workspace is None:
+        n = extract_workspace_bytes(B, s_t, s_r, s_i, H, D)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+    axes, na = _axes_array(axes_dims)
+    rc = lib.flux_joint_rope_attention_extract(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(ref_ids), s_r, _ptr(img_ids), s_i, B,
+        H, D, axes, na, float(theta), _ptr(out), _ptr(cache_k), _ptr(cache_v), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention_extract", rc, lib)
+    return out, cache_k, cache_v
+
+
+def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES_DIMS,
+                     theta=THETA, out=None, workspace=None, stream=None):
+    """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; returns out."""
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v), ("cache_k", cache_k), ("cache_v", cache_v)):
+        _need_cuda(name, t, torch.bfloat16)
+    B, S, H, D = q.shape
+    s_t, s_i, s_r = _rows(txt_ids), _rows(img_ids), int(cache_k.shape[1])
+    for name, t in (("txt_ids", txt_ids), ("img_ids", img_ids)):
+        if t is not None and t.numel() > 0:
+            _need_cuda(name, t, torch.int32)
+    out = torch.empty_like(q) if out is None else out
+    if workspace is None:
+        n = cached_workspace_bytes(B, s_t, s_i, s_r, H, D)
+        workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
+    axes, na = _axes_array(axes_dims)
+    rc = lib.flux_joint_rope_attention_cached(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(img_ids), s_i, _ptr(cache_k),
+        _ptr(cache_v), s_r, B, H, D, axes, na, float(theta), _ptr(out), _ptr(workspace),
+        workspace.numel(), _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention_cached", rc, lib)
     return out
 
 

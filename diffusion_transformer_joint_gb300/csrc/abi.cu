@@ -254,6 +254,235 @@ int flux_joint_qknorm_rope_attention_tabled(const void *q, const void *k, const 
                 stream);
 }
 
+// ---------------------------------------------- reference-image KV modes
+
+namespace {
+
+size_t pad256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
+
+// Segments of extract mode over tokens [txt ; ref ; img]: text and image
+// queries over every key (key range 0), reference queries over the
+// reference keys (key range 1). Returns the number of segments.
+int extract_segments(int64_t S_txt, int64_t S_ref, int64_t S_img, flux::AttnSegment *sg) {
+  const int64_t S = S_txt + S_ref + S_img;
+  int n = 0;
+  if (S_txt > 0) sg[n++] = {0, S_txt, 0, S, 0};
+  if (S_img > 0) sg[n++] = {S_txt + S_ref, S, 0, S, 0};
+  if (S_ref > 0) sg[n++] = {S_txt, S_txt + S_ref, S_txt, S_txt + S_ref, 1};
+  return n;
+}
+
+bool kv_shape_ok(int B, int H, int D, int64_t S) {
+  return D == 128 && B >= 1 && H >= 1 && S >= 1 && S <= 0x7FFFFFFFLL && B <= 65535 &&
+         H <= 65535 && static_cast<int64_t>(B) * H * ((S + 127) / 128) <= 0x3FFFFFFFLL;
+}
+
+}  // namespace
+
+size_t flux_joint_rope_attention_extract_workspace(int B, int64_t S_txt, int64_t S_ref,
+                                                   int64_t S_img, int H, int D) {
+  if (S_txt < 0 || S_ref < 0 || S_img < 0 || !kv_shape_ok(B, H, D, S_txt + S_ref + S_img))
+    return 0;
+  const int64_t S = S_txt + S_ref + S_img;
+  flux::AttnSegment sg[flux::kMaxSegments];
+  const int n = extract_segments(S_txt, S_ref, S_img, sg);
+  return flux::kStatusBytes + flux::packed_table_bytes(S, D) +
+         flux::exchange_bytes(B, S, S, H, sg, n);
+}
+
+int flux_joint_rope_attention_extract(const void *q, const void *k, const void *v,
+                                      const int32_t *txt_ids, int64_t S_txt,
+                                      const int32_t *ref_ids, int64_t S_ref,
+                                      const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                      const int32_t *axes_dims, int n_axes, double theta,
+                                      void *out, void *cache_k, void *cache_v, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
+    return FLUX_ERR_NULL;
+  if ((S_txt > 0 && txt_ids == nullptr) || (S_ref > 0 && ref_ids == nullptr) ||
+      (S_img > 0 && img_ids == nullptr) || (S_ref > 0 && (cache_k == nullptr || cache_v == nullptr)))
+    return FLUX_ERR_NULL;
+  if (S_txt < 0 || S_ref < 0 || S_img < 0) return FLUX_ERR_SHAPE;
+  const int64_t S = S_txt + S_ref + S_img;
+  if (!kv_shape_ok(B, H, D, S)) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  if (2 * pp.n_pairs != D) return FLUX_ERR_AXES;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (S_ref > 0 && (!aligned16(cache_k) || !aligned16(cache_v))))
+    return FLUX_ERR_ALIGN;
+  const size_t row = static_cast<size_t>(H) * D * 2;  // bytes of one token of all heads
+  const size_t tb = static_cast<size_t>(B) * S * row;
+  const size_t cb = static_cast<size_t>(B) * S_ref * row;
+  const size_t need = flux_joint_rope_attention_extract_workspace(B, S_txt, S_ref, S_img, H, D);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < need)
+    return FLUX_ERR_WORKSPACE;
+  const void *ins[3] = {q, k, v};
+  for (const void *x : ins)
+    if (overlaps(out, tb, x, tb) || overlaps(workspace, need, x, tb) ||
+        (cb > 0 && (overlaps(cache_k, cb, x, tb) || overlaps(cache_v, cb, x, tb))))
+      return FLUX_ERR_ALIAS;
+  if (overlaps(workspace, need, out, tb) ||
+      (cb > 0 && (overlaps(cache_k, cb, out, tb) || overlaps(cache_v, cb, out, tb) ||
+                  overlaps(cache_k, cb, cache_v, cb) || overlaps(workspace, need, cache_k, cb) ||
+                  overlaps(workspace, need, cache_v, cb))))
+    return FLUX_ERR_ALIAS;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
+  void *xbuf = ws + flux::kStatusBytes + flux::packed_table_bytes(S, D);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
+  // the table of [txt ; ref ; img]: two launches of the two-segment table kernel
+  if (flux::launch_rope_tables(txt_ids, S_txt, ref_ids, S_ref, pp, flux::TableFormat::kPackedF16,
+                               nullptr, nullptr, table, st) != cudaSuccess ||
+      (S_img > 0 &&
+       flux::launch_rope_tables(img_ids, S_img, nullptr, 0, pp, flux::TableFormat::kPackedF16,
+                                nullptr, nullptr, table + (S_txt + S_ref) * (D / 2), st) !=
+           cudaSuccess))
+    return FLUX_ERR_CUDA;
+  flux::AttnSegment sg[flux::kMaxSegments];
+  const int n = extract_segments(S_txt, S_ref, S_img, sg);
+  if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, sg, n, xbuf,
+                                      nullptr, st) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  if (S_ref > 0) {
+    // the cache: every key tile was rotated once into the exchange buffer's
+    // K copy (each is loaded by some item of a key range covering it)
+    size_t flags = 0;
+    {
+      flux::AttnSegment one[flux::kMaxSegments];
+      const int m = extract_segments(S_txt, S_ref, S_img, one);
+      flags = flux::exchange_bytes(B, S, S, H, one, m) - 2 * tb;
+    }
+    const uint8_t *krot = static_cast<const uint8_t *>(xbuf) + flags;
+    const size_t width = static_cast<size_t>(S_ref) * row, pitch = static_cast<size_t>(S) * row;
+    if (cudaMemcpy2DAsync(cache_k, width, krot + S_txt * row, pitch, width, B,
+                          cudaMemcpyDeviceToDevice, st) != cudaSuccess ||
+        cudaMemcpy2DAsync(cache_v, width, static_cast<const uint8_t *>(v) + S_txt * row, pitch,
+                          width, B, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return FLUX_ERR_CUDA;
+  }
+  return FLUX_OK;
+}
+
+size_t flux_joint_rope_attention_cached_workspace(int B, int64_t S_txt, int64_t S_img,
+                                                  int64_t S_ref, int H, int D) {
+  if (S_txt < 0 || S_img < 0 || S_ref < 0 || S_txt + S_img < 1 ||
+      !kv_shape_ok(B, H, D, S_txt + S_img + S_ref))
+    return 0;
+  const int64_t S_q = S_txt + S_img, S_k = S_q + S_ref;
+  const flux::AttnSegment all{0, S_q, 0, S_k, 0};
+  const size_t kv = static_cast<size_t>(B) * S_k * H * D * 2;
+  return flux::kStatusBytes + flux::packed_table_bytes(S_q, D) + flux::packed_table_bytes(S_k, D) +
+         pad256(static_cast<size_t>(S_ref) * 8 * sizeof(int32_t)) + 2 * pad256(kv) +
+         flux::exchange_bytes(B, S_q, S_k, H, &all, 1);
+}
+
+int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v,
+                                     const int32_t *txt_ids, int64_t S_txt,
+                                     const int32_t *img_ids, int64_t S_img, const void *cache_k,
+                                     const void *cache_v, int64_t S_ref, int B, int H, int D,
+                                     const int32_t *axes_dims, int n_axes, double theta,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
+    return FLUX_ERR_NULL;
+  if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr) ||
+      (S_ref > 0 && (cache_k == nullptr || cache_v == nullptr)))
+    return FLUX_ERR_NULL;
+  if (S_txt < 0 || S_img < 0 || S_ref < 0 || S_txt + S_img < 1) return FLUX_ERR_SHAPE;
+  const int64_t S_q = S_txt + S_img, S_k = S_q + S_ref;
+  if (!kv_shape_ok(B, H, D, S_k)) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  if (2 * pp.n_pairs != D) return FLUX_ERR_AXES;
+  if (n_axes > 8) return FLUX_ERR_AXES;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (S_ref > 0 && (!aligned16(cache_k) || !aligned16(cache_v))))
+    return FLUX_ERR_ALIGN;
+  const size_t row = static_cast<size_t>(H) * D * 2;
+  const size_t tb = static_cast<size_t>(B) * S_q * row;
+  const size_t cb = static_cast<size_t>(B) * S_ref * row;
+  const size_t need = flux_joint_rope_attention_cached_workspace(B, S_txt, S_img, S_ref, H, D);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < need)
+    return FLUX_ERR_WORKSPACE;
+  const void *ins[5] = {q, k, v, cache_k, cache_v};
+  const size_t sz[5] = {tb, tb, tb, cb, cb};
+  for (int i = 0; i < 5; ++i)
+    if (sz[i] > 0 && (overlaps(out, tb, ins[i], sz[i]) || overlaps(workspace, need, ins[i], sz[i])))
+      return FLUX_ERR_ALIAS;
+  if (overlaps(workspace, need, out, tb)) return FLUX_ERR_ALIAS;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+
+  // workspace: status | table of [txt ; img] | table of [txt ; ref ; img]
+  // (identity rows for the cached, already rotated keys) | zero ids |
+  // K and V of [txt ; ref ; img] | exchange buffer
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  size_t off = flux::kStatusBytes;
+  uint32_t *table_q = reinterpret_cast<uint32_t *>(ws + off);
+  off += flux::packed_table_bytes(S_q, D);
+  uint32_t *table_k = reinterpret_cast<uint32_t *>(ws + off);
+  off += flux::packed_table_bytes(S_k, D);
+  int32_t *zero_ids = reinterpret_cast<int32_t *>(ws + off);
+  off += pad256(static_cast<size_t>(S_ref) * 8 * sizeof(int32_t));
+  const size_t kv = static_cast<size_t>(B) * S_k * row;
+  uint8_t *k_cat = ws + off;
+  off += pad256(kv);
+  uint8_t *v_cat = ws + off;
+  off += pad256(kv);
+  void *xbuf = ws + off;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
+  const int P = D / 2;
+  if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
+                               nullptr, nullptr, table_q, st) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  // K-side table: txt rows, identity rows (all-zero ids), image rows
+  if (S_ref > 0 &&
+      cudaMemsetAsync(zero_ids, 0, static_cast<size_t>(S_ref) * n_axes * sizeof(int32_t), st) !=
+          cudaSuccess)
+    return FLUX_ERR_CUDA;
+  if (flux::launch_rope_tables(txt_ids, S_txt, zero_ids, S_ref, pp, flux::TableFormat::kPackedF16,
+                               nullptr, nullptr, table_k, st) != cudaSuccess ||
+      (S_img > 0 &&
+       flux::launch_rope_tables(img_ids, S_img, nullptr, 0, pp, flux::TableFormat::kPackedF16,
+                                nullptr, nullptr, table_k + (S_txt + S_ref) * P, st) !=
+           cudaSuccess))
+    return FLUX_ERR_CUDA;
+  // K and V of [txt ; ref ; img], one strided copy per block
+  const size_t pk = static_cast<size_t>(S_k) * row, pq = static_cast<size_t>(S_q) * row;
+  const uint8_t *srcs[2] = {static_cast<const uint8_t *>(k), static_cast<const uint8_t *>(v)};
+  const uint8_t *caches[2] = {static_cast<const uint8_t *>(cache_k),
+                              static_cast<const uint8_t *>(cache_v)};
+  uint8_t *dsts[2] = {k_cat, v_cat};
+  for (int i = 0; i < 2; ++i) {
+    if ((S_txt > 0 && cudaMemcpy2DAsync(dsts[i], pk, srcs[i], pq, S_txt * row, B,
+                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess) ||
+        (S_ref > 0 && cudaMemcpy2DAsync(dsts[i] + S_txt * row, pk, caches[i], S_ref * row,
+                                        S_ref * row, B, cudaMemcpyDeviceToDevice, st) !=
+                          cudaSuccess) ||
+        (S_img > 0 && cudaMemcpy2DAsync(dsts[i] + (S_txt + S_ref) * row, pk,
+                                        srcs[i] + S_txt * row, pq, S_img * row, B,
+                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess))
+      return FLUX_ERR_CUDA;
+  }
+  const flux::AttnSegment all{0, S_q, 0, S_k, 0};
+  if (flux::launch_attention_segments(q, k_cat, v_cat, out, table_q, table_k, status, B, S_q, S_k,
+                                      H, &all, 1, xbuf, nullptr, st) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return FLUX_OK;
+}
+
 int flux_query_status(const void *workspace, void *stream) {
   if (workspace == nullptr) return FLUX_ERR_NULL;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -231,6 +231,57 @@ int flux_joint_qknorm_rope_attention_tabled(const void *q, const void *k, const 
                                             int32_t *status, void *krot_scratch,
                                             size_t krot_bytes, void *stream);
 
+/*
+ * Reference-image KV modes ("Diffusers 中 Flux2Transformer2DModel 全面解析",
+ * section 参考图 KV 缓存机制). The cache holds the reference tokens' K after
+ * RoPE and their V, bf16 [B, S_ref, H, D] each.
+ *
+ * flux_joint_rope_attention_extract: tokens [txt ; ref ; img] (the order of
+ * the extract mode; q, k, v, out are [B, S, H, D] with S = S_txt + S_ref +
+ * S_img, ids given per segment, each [S_seg, n_axes], NULL when empty).
+ * Reference queries attend to the reference keys only; text and image
+ * queries attend to every key. cache_k / cache_v (device, [B, S_ref, H, D],
+ * 16-byte aligned, not overlapping anything else; may be NULL when S_ref is
+ * 0) receive the reference tokens' rotated K (the bf16 values the kernel
+ * used) and their V.
+ *   workspace  >= flux_joint_rope_attention_extract_workspace(B, S_txt, S_ref,
+ *              S_img, H, D) bytes, 256-byte aligned (status word first, as for
+ *              flux_query_status).
+ * Other arguments and return codes as flux_joint_rope_attention.
+ */
+size_t flux_joint_rope_attention_extract_workspace(int B, int64_t S_txt, int64_t S_ref,
+                                                   int64_t S_img, int H, int D);
+int flux_joint_rope_attention_extract(const void *q, const void *k, const void *v,
+                                      const int32_t *txt_ids, int64_t S_txt,
+                                      const int32_t *ref_ids, int64_t S_ref,
+                                      const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                      const int32_t *axes_dims, int n_axes, double theta,
+                                      void *out, void *cache_k, void *cache_v, void *workspace,
+                                      size_t workspace_bytes, void *stream);
+
+/*
+ * flux_joint_rope_attention_cached: the cached mode. q, k, v, out are
+ * [B, S_txt + S_img, H, D] for the tokens [txt ; img]; every query attends to
+ * the keys [txt ; cached ref ; img] and the values in the same order. The
+ * cached K is used as stored (already rotated, not rotated again).
+ *   cache_k, cache_v  device [B, S_ref, H, D] bf16, 16-byte aligned, as
+ *                     written by flux_joint_rope_attention_extract.
+ *   workspace  >= flux_joint_rope_attention_cached_workspace(B, S_txt, S_img,
+ *              S_ref, H, D) bytes, 256-byte aligned. It holds, besides the
+ *              status word and tables, the keys and values gathered in the
+ *              order [txt ; ref ; img].
+ * Other arguments and return codes as flux_joint_rope_attention.
+ */
+size_t flux_joint_rope_attention_cached_workspace(int B, int64_t S_txt, int64_t S_img,
+                                                  int64_t S_ref, int H, int D);
+int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v,
+                                     const int32_t *txt_ids, int64_t S_txt,
+                                     const int32_t *img_ids, int64_t S_img, const void *cache_k,
+                                     const void *cache_v, int64_t S_ref, int B, int H, int D,
+                                     const int32_t *axes_dims, int n_axes, double theta,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
  * on every device that loads this library, held until the process exits. */

@@ -105,11 +105,11 @@ class Oracle:
         lib.oracle_joint_qknorm_rope_attention.restype = ctypes.c_int
         lib.oracle_attention_extract.argtypes = [
             P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
-            ctypes.c_double, ctypes.c_int64, ctypes.c_int64, P, P, P]
+            ctypes.c_double, ctypes.c_int64, ctypes.c_int64, P, ctypes.c_int64, P, P, P]
         lib.oracle_attention_extract.restype = ctypes.c_int
         lib.oracle_attention_cached.argtypes = [
             P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
-            ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P]
+            ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P, ctypes.c_int64, P]
         lib.oracle_attention_cached.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
@@ -196,9 +196,9 @@ class Oracle:
 
 
     def attention_extract(self, q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                          theta=2000.0):
-        """Extract mode over tokens [txt ; ref ; img]: (out [B, S, H, D], cache_k,
-        cache_v [B, S_ref, H, D]) in fp64."""
+                          theta=2000.0, rows=None):
+        """Extract mode over tokens [txt ; ref ; img]: (out [B, len(rows) or S, H, D],
+        cache_k, cache_v [B, S_ref, H, D]) in fp64."""
         q = np.ascontiguousarray(q, dtype=np.float64)
         k = np.ascontiguousarray(k, dtype=np.float64)
         v = np.ascontiguousarray(v, dtype=np.float64)
@@ -208,18 +208,21 @@ class Oracle:
         n_r = 0 if ref_ids is None else np.asarray(ref_ids).reshape(-1, axes.size).shape[0]
         ids = joint_ids(joint_ids(txt_ids, ref_ids) if n_t + n_r else None, img_ids)
         assert ids.shape[0] == S
-        out = np.empty_like(q)
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n_out = S if rows_arr is None else rows_arr.size
+        out = np.empty((B, n_out, H, D))
         ck = np.empty((B, n_r, H, D))
         cv = np.empty((B, n_r, H, D))
-        rc = self.lib.oracle_attention_extract(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids),
-                                               _ptr(axes), axes.size, float(theta), n_t, n_r,
-                                               _ptr(out), _ptr(ck), _ptr(cv))
+        rc = self.lib.oracle_attention_extract(
+            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size, float(theta),
+            n_t, n_r, None if rows_arr is None else _ptr(rows_arr), n_out, _ptr(out), _ptr(ck),
+            _ptr(cv))
         if rc != 0:
             raise ValueError("oracle_attention_extract: bad arguments")
         return out, ck, cv
 
     def attention_cached(self, q, k, v, txt_ids, img_ids, cache_k, cache_v,
-                         axes_dims=(32, 32, 32, 32), theta=2000.0):
+                         axes_dims=(32, 32, 32, 32), theta=2000.0, rows=None):
         """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; fp64 out."""
         q = np.ascontiguousarray(q, dtype=np.float64)
         k = np.ascontiguousarray(k, dtype=np.float64)
@@ -231,10 +234,13 @@ class Oracle:
         n_t = 0 if txt_ids is None else np.asarray(txt_ids).reshape(-1, axes.size).shape[0]
         ids = joint_ids(txt_ids, img_ids)
         assert ids.shape[0] == S and ck.shape == cv.shape and ck.shape[0] == B
-        out = np.empty_like(q)
-        rc = self.lib.oracle_attention_cached(_ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids),
-                                              _ptr(axes), axes.size, float(theta), n_t, _ptr(ck),
-                                              _ptr(cv), ck.shape[1], _ptr(out))
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n_out = S if rows_arr is None else rows_arr.size
+        out = np.empty((B, n_out, H, D))
+        rc = self.lib.oracle_attention_cached(
+            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size, float(theta),
+            n_t, _ptr(ck), _ptr(cv), ck.shape[1], None if rows_arr is None else _ptr(rows_arr),
+            n_out, _ptr(out))
         if rc != 0:
             raise ValueError("oracle_attention_cached: bad arguments")
         return out
@@ -261,14 +267,14 @@ def rms_norm(x, w, eps=1e-6):
 
 
 def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                      theta=2000.0):
-    return default().attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims, theta)
+                      theta=2000.0, rows=None):
+    return default().attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims, theta, rows)
 
 
 def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=(32, 32, 32, 32),
-                     theta=2000.0):
+                     theta=2000.0, rows=None):
     return default().attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims,
-                                      theta)
+                                      theta, rows)
 
 
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),

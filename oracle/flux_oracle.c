@@ -314,15 +314,16 @@ static void attend_range(const double *qhat, const double *khat, const double *c
 }
 
 /* Extract mode. Tokens [txt ; ref ; img] (S_txt, S_ref, then the rest), ids
- * [S, n_axes] in the same order. out [B, S, H, D]: reference queries attend
- * to the reference keys, every other query to all S keys. cache_k / cache_v
- * [B, S_ref, H, D]: the reference tokens' rotated K and their V. Single
- * threaded. Returns 0, or -1 on bad arguments. */
+ * [S, n_axes] in the same order. Reference queries attend to the reference
+ * keys, every other query to all S keys; out [B, n_rows, H, D] for the query
+ * tokens rows[0 .. n_rows) (every token when rows is NULL). cache_k /
+ * cache_v [B, S_ref, H, D]: the reference tokens' rotated K and their V.
+ * Single threaded. Returns 0, or -1 on bad arguments. */
 int oracle_attention_extract(const double *q, const double *k, const double *v, int B,
                              int64_t S, int H, int D, const int32_t *ids,
                              const int32_t *axes_dims, int n_axes, double theta,
-                             int64_t S_txt, int64_t S_ref, double *out, double *cache_k,
-                             double *cache_v) {
+                             int64_t S_txt, int64_t S_ref, const int64_t *rows, int64_t n_rows,
+                             double *out, double *cache_k, double *cache_v) {
   int sum = 0;
   for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
   if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0 || S_txt < 0 || S_ref < 0 ||
@@ -347,12 +348,14 @@ int oracle_attention_extract(const double *q, const double *k, const double *v, 
                               khat + j * D);
         vrows[j] = v + off;
       }
-      for (int64_t i = 0; i < S; ++i) {
+      for (int64_t r = 0; r < (rows ? n_rows : S); ++r) {
+        const int64_t i = rows ? rows[r] : r;
         const int64_t off = (((int64_t)b * S + i) * H + h) * D;
+        const int64_t ooff = (((int64_t)b * (rows ? n_rows : S) + r) * H + h) * D;
         oracle_rope_apply_vec(q + off, cos_t + i * (D / 2), sin_t + i * (D / 2), D, qhat);
         const int is_ref = i >= S_txt && i < S_txt + S_ref;
         attend_range(qhat, khat, vrows, is_ref ? S_txt : 0, is_ref ? S_txt + S_ref : S, D, z,
-                     out + off);
+                     out + ooff);
       }
       for (int64_t r = 0; r < S_ref; ++r) {
         const int64_t coff = (((int64_t)b * S_ref + r) * H + h) * D;
@@ -374,13 +377,14 @@ int oracle_attention_extract(const double *q, const double *k, const double *v, 
 /* Cached mode. Queries, keys and values of the tokens [txt ; img] (S_txt,
  * then the rest; ids [S, n_axes] in that order) and a cache [B, S_ref, H, D]
  * of reference keys (already rotated) and values. Every query attends to the
- * keys [txt ; cached ref ; img]. out [B, S, H, D]. Single threaded. Returns
- * 0, or -1 on bad arguments. */
+ * keys [txt ; cached ref ; img]. out [B, n_rows, H, D] for the query tokens
+ * rows[0 .. n_rows) (every token when rows is NULL). Single threaded.
+ * Returns 0, or -1 on bad arguments. */
 int oracle_attention_cached(const double *q, const double *k, const double *v, int B,
                             int64_t S, int H, int D, const int32_t *ids,
                             const int32_t *axes_dims, int n_axes, double theta, int64_t S_txt,
                             const double *cache_k, const double *cache_v, int64_t S_ref,
-                            double *out) {
+                            const int64_t *rows, int64_t n_rows, double *out) {
   int sum = 0;
   for (int a = 0; a < n_axes; ++a) sum += axes_dims[a];
   if (sum != D || D % 2 != 0 || S <= 0 || B <= 0 || H <= 0 || S_txt < 0 || S_txt > S ||
@@ -414,10 +418,12 @@ int oracle_attention_cached(const double *q, const double *k, const double *v, i
           vrows[j] = v + off;
         }
       }
-      for (int64_t i = 0; i < S; ++i) {
+      for (int64_t r = 0; r < (rows ? n_rows : S); ++r) {
+        const int64_t i = rows ? rows[r] : r;
         const int64_t off = (((int64_t)b * S + i) * H + h) * D;
+        const int64_t ooff = (((int64_t)b * (rows ? n_rows : S) + r) * H + h) * D;
         oracle_rope_apply_vec(q + off, cos_t + i * (D / 2), sin_t + i * (D / 2), D, qhat);
-        attend_range(qhat, khat, vrows, 0, Sk, D, z, out + off);
+        attend_range(qhat, khat, vrows, 0, Sk, D, z, out + ooff);
       }
     }
   free(khat);

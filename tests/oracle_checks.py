@@ -396,6 +396,13 @@ def check_extract_then_cached_reproduces_rows(orc):
     keep = np.r_[0:n_t, n_t + n_r:S]
     out2 = orc.attention_cached(q[:, keep], k[:, keep], v[:, keep], txt, img, ck, cv)
     assert np.allclose(out2, out[:, keep], rtol=0, atol=1e-12)
+    # row subsets give the same rows
+    rows = np.array([S - 1, 0, n_t + 3, n_t])
+    sub, ck2, _ = orc.attention_extract(q, k, v, txt, ref, img, rows=rows)
+    assert np.array_equal(sub, out[:, rows]) and np.array_equal(ck2, ck)
+    sub2 = orc.attention_cached(q[:, keep], k[:, keep], v[:, keep], txt, img, ck, cv,
+                                rows=np.array([2, 0]))
+    assert np.array_equal(sub2, out2[:, [2, 0]])
 
 
 ALL_CHECKS = [

@@ -160,3 +160,33 @@ def test_qknorm_arguments_checked_on_host(lib):
 
     assert tab(81) == -2
     assert tab(-1) == -2
+
+
+def test_kv_mode_workspace_sizes_and_checks(lib):
+    P = ctypes.c_void_p
+    assert lib.flux_joint_rope_attention_extract_workspace(1, 512, 8192, 4096, 32, 128) > 0
+    assert lib.flux_joint_rope_attention_extract_workspace(1, 0, 0, 0, 32, 128) == 0
+    assert lib.flux_joint_rope_attention_extract_workspace(1, 5, 5, 5, 32, 64) == 0
+    assert lib.flux_joint_rope_attention_cached_workspace(1, 512, 4096, 8192, 32, 128) > 0
+    assert lib.flux_joint_rope_attention_cached_workspace(1, 0, 0, 8, 32, 128) == 0
+    axes = (ctypes.c_int32 * 4)(32, 32, 32, 32)
+    need = lib.flux_joint_rope_attention_extract_workspace(1, 16, 32, 32, 2, 128)
+
+    def extract(ck=96 * 1024 * 1024, ws=256 * 65536, wsb=None, ref_ids=3072):
+        return lib.flux_joint_rope_attention_extract(
+            P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(ref_ids) if ref_ids else None, 32,
+            P(2048), 32, 1, 2, 128, axes, 4, 2000.0, P(48 * 1024 * 1024), P(ck) if ck else None,
+            P(100 * 1024 * 1024), P(ws), need if wsb is None else wsb, None)
+
+    assert extract(ck=0) == -1            # cache needed when S_ref > 0
+    assert extract(ref_ids=0) == -1       # ids needed for a non-empty segment
+    assert extract(wsb=need - 1) == -5    # workspace too small
+    assert extract(ck=16) == -9           # cache overlaps q
+    cneed = lib.flux_joint_rope_attention_cached_workspace(1, 16, 32, 8, 2, 128)
+    assert lib.flux_joint_rope_attention_cached(
+        P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(2048), 32, None, P(200 * 1024), 8, 1,
+        2, 128, axes, 4, 2000.0, P(48 * 1024 * 1024), P(256 * 65536), cneed, None) == -1
+    assert lib.flux_joint_rope_attention_cached(
+        P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(2048), 32, P(300 * 1024),
+        P(200 * 1024 + 8), 8, 1, 2, 128, axes, 4, 2000.0, P(48 * 1024 * 1024), P(256 * 65536),
+        cneed, None) == -4
