@@ -14,8 +14,8 @@ exchange (heads and batches are independent): weak scaling, and `value` is
 all ranks' FLOPs over the slowest rank's time.
 
 `--kv-mode extract|cached` times one reference-image KV-mode call per step on
-the two-reference edit shape instead (tables, attention and the cache copies
-or key/value gathers inside the call).
+the two-reference edit shape instead (tables, attention and, for extract, the
+cache copies inside the call).
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload.
@@ -525,7 +525,7 @@ def run_kv(args, rank, world, local_rank):
                   f"({n_sets * set_bytes / 2**20:.0f} MiB > 129 MiB L2)",
             "step": ("two table kernels, the attention kernel over 3 segments, two cache copies"
                      if mode == "extract" else
-                     "two table kernels, two key/value gathers, the attention kernel"),
+                     "one table kernel, the attention kernel (cache read in place, not rotated)"),
         },
         "roofline": {
             "bound": "tensor", "kernel": "whole call (tables + attention + copies)",
@@ -540,7 +540,7 @@ def run_kv(args, rank, world, local_rank):
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in + h_ids),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
                 "api": f"flux_joint_rope_attention_{mode}"},
-        "gpu_launches": 3 * K,
+        "gpu_launches": (3 if mode == "extract" else 2) * K,
     }
 
 

@@ -266,9 +266,9 @@ size_t pad256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 int extract_segments(int64_t S_txt, int64_t S_ref, int64_t S_img, flux::AttnSegment *sg) {
   const int64_t S = S_txt + S_ref + S_img;
   int n = 0;
-  if (S_txt > 0) sg[n++] = {0, S_txt, 0, S, 0};
-  if (S_img > 0) sg[n++] = {S_txt + S_ref, S, 0, S, 0};
-  if (S_ref > 0) sg[n++] = {S_txt, S_txt + S_ref, S_txt, S_txt + S_ref, 1};
+  if (S_txt > 0) sg[n++] = {0, S_txt, 0, S, 0, 0};
+  if (S_img > 0) sg[n++] = {S_txt + S_ref, S, 0, S, 0, 0};
+  if (S_ref > 0) sg[n++] = {S_txt, S_txt + S_ref, S_txt, S_txt + S_ref, 1, 0};
   return n;
 }
 
@@ -348,8 +348,8 @@ int flux_joint_rope_attention_extract(const void *q, const void *k, const void *
     return FLUX_ERR_CUDA;
   flux::AttnSegment sg[flux::kMaxSegments];
   const int n = extract_segments(S_txt, S_ref, S_img, sg);
-  if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, sg, n, xbuf,
-                                      nullptr, st) != cudaSuccess)
+  if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, sg, n,
+                                      nullptr, xbuf, nullptr, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   if (S_ref > 0) {
     // the cache: every key tile was rotated once into the exchange buffer's
@@ -376,12 +376,10 @@ size_t flux_joint_rope_attention_cached_workspace(int B, int64_t S_txt, int64_t 
   if (S_txt < 0 || S_img < 0 || S_ref < 0 || S_txt + S_img < 1 ||
       !kv_shape_ok(B, H, D, S_txt + S_img + S_ref))
     return 0;
-  const int64_t S_q = S_txt + S_img, S_k = S_q + S_ref;
-  const flux::AttnSegment all{0, S_q, 0, S_k, 0};
-  const size_t kv = static_cast<size_t>(B) * S_k * H * D * 2;
-  return flux::kStatusBytes + flux::packed_table_bytes(S_q, D) + flux::packed_table_bytes(S_k, D) +
-         pad256(static_cast<size_t>(S_ref) * 8 * sizeof(int32_t)) + 2 * pad256(kv) +
-         flux::exchange_bytes(B, S_q, S_k, H, &all, 1);
+  const int64_t S_q = S_txt + S_img;
+  const flux::AttnSegment all{0, S_q, 0, S_q, 0, S_ref};
+  return flux::kStatusBytes + flux::packed_table_bytes(S_q, D) +
+         flux::exchange_bytes(B, S_q, S_q, H, &all, 1);
 }
 
 int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v,
@@ -423,62 +421,22 @@ int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v
   const int dc = check_device();
   if (dc != FLUX_OK) return dc;
 
-  // workspace: status | table of [txt ; img] | table of [txt ; ref ; img]
-  // (identity rows for the cached, already rotated keys) | zero ids |
-  // K and V of [txt ; ref ; img] | exchange buffer
+  // workspace: status | table of [txt ; img] | exchange buffer. The keys are
+  // [txt ; img] from k, rotated here, then the cache's rows, rotated already
+  // (key order does not change non-causal attention).
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   int *status = reinterpret_cast<int *>(ws);
-  size_t off = flux::kStatusBytes;
-  uint32_t *table_q = reinterpret_cast<uint32_t *>(ws + off);
-  off += flux::packed_table_bytes(S_q, D);
-  uint32_t *table_k = reinterpret_cast<uint32_t *>(ws + off);
-  off += flux::packed_table_bytes(S_k, D);
-  int32_t *zero_ids = reinterpret_cast<int32_t *>(ws + off);
-  off += pad256(static_cast<size_t>(S_ref) * 8 * sizeof(int32_t));
-  const size_t kv = static_cast<size_t>(B) * S_k * row;
-  uint8_t *k_cat = ws + off;
-  off += pad256(kv);
-  uint8_t *v_cat = ws + off;
-  off += pad256(kv);
-  void *xbuf = ws + off;
+  uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
+  void *xbuf = ws + flux::kStatusBytes + flux::packed_table_bytes(S_q, D);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
-  const int P = D / 2;
   if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
-                               nullptr, nullptr, table_q, st) != cudaSuccess)
+                               nullptr, nullptr, table, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
-  // K-side table: txt rows, identity rows (all-zero ids), image rows
-  if (S_ref > 0 &&
-      cudaMemsetAsync(zero_ids, 0, static_cast<size_t>(S_ref) * n_axes * sizeof(int32_t), st) !=
-          cudaSuccess)
-    return FLUX_ERR_CUDA;
-  if (flux::launch_rope_tables(txt_ids, S_txt, zero_ids, S_ref, pp, flux::TableFormat::kPackedF16,
-                               nullptr, nullptr, table_k, st) != cudaSuccess ||
-      (S_img > 0 &&
-       flux::launch_rope_tables(img_ids, S_img, nullptr, 0, pp, flux::TableFormat::kPackedF16,
-                                nullptr, nullptr, table_k + (S_txt + S_ref) * P, st) !=
-           cudaSuccess))
-    return FLUX_ERR_CUDA;
-  // K and V of [txt ; ref ; img], one strided copy per block
-  const size_t pk = static_cast<size_t>(S_k) * row, pq = static_cast<size_t>(S_q) * row;
-  const uint8_t *srcs[2] = {static_cast<const uint8_t *>(k), static_cast<const uint8_t *>(v)};
-  const uint8_t *caches[2] = {static_cast<const uint8_t *>(cache_k),
-                              static_cast<const uint8_t *>(cache_v)};
-  uint8_t *dsts[2] = {k_cat, v_cat};
-  for (int i = 0; i < 2; ++i) {
-    if ((S_txt > 0 && cudaMemcpy2DAsync(dsts[i], pk, srcs[i], pq, S_txt * row, B,
-                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess) ||
-        (S_ref > 0 && cudaMemcpy2DAsync(dsts[i] + S_txt * row, pk, caches[i], S_ref * row,
-                                        S_ref * row, B, cudaMemcpyDeviceToDevice, st) !=
-                          cudaSuccess) ||
-        (S_img > 0 && cudaMemcpy2DAsync(dsts[i] + (S_txt + S_ref) * row, pk,
-                                        srcs[i] + S_txt * row, pq, S_img * row, B,
-                                        cudaMemcpyDeviceToDevice, st) != cudaSuccess))
-      return FLUX_ERR_CUDA;
-  }
-  const flux::AttnSegment all{0, S_q, 0, S_k, 0};
-  if (flux::launch_attention_segments(q, k_cat, v_cat, out, table_q, table_k, status, B, S_q, S_k,
-                                      H, &all, 1, xbuf, nullptr, st) != cudaSuccess)
+  const flux::AttnSegment all{0, S_q, 0, S_q, 0, S_ref};
+  const flux::PreRotatedKV cache{cache_k, cache_v, S_ref};
+  if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S_q, S_q, H, &all, 1,
+                                      &cache, xbuf, nullptr, st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }

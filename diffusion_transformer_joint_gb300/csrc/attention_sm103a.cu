@@ -297,31 +297,35 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
   }
 }
 
+// kpre / vpre: keys and values that arrive rotated already (a reference-image
+// cache), appended to a segment's key range.
 struct Maps {
-  CUtensorMap q, k, v, out, krot, qrot, table_q, table_k;
+  CUtensorMap q, k, v, out, krot, qrot, table_q, table_k, kpre, vpre;
 };
 
 // A work item: batch b, head h, the 256 query rows from m0 (rows of Q / out
 // at or past q_hi belong to another segment: computed, never stored), its key
-// range [k_lo, k_hi) of K / V in n_tiles 128-key tiles walked from tile j0,
-// and the publication flags of that key range for (b, h) ([n_tiles][4]; null
-// without the exchange buffer).
+// range: rows [k_lo, k_hi) of K / V in n_main 128-key tiles, then rows
+// [0, n_pre) of the pre-rotated K / V in the remaining tiles of n_tiles, all
+// walked from tile j0; and the publication flags of the n_main tiles for
+// (b, h) ([n_main][4]; null without the exchange buffer).
 struct Item {
-  int b, h, n_tiles, j0;
-  int64_t m0, q_hi, k_lo, k_hi;
+  int b, h, n_tiles, n_main, j0;
+  int64_t m0, q_hi, k_lo, k_hi, n_pre;
   uint64_t *flags;
 };
 
 // The segments of one launch, by value: segment g owns items
 // [first_item[g], first_item[g + 1]), queries [q_lo, q_hi) in n_rb 256-row
-// blocks and keys [k_lo, k_hi) in n_tiles tiles; flag_off is the word offset
-// of its key range's flags in the exchange buffer.
+// blocks, keys [k_lo, k_hi) in n_main tiles and n_pre pre-rotated keys, n_tiles
+// tiles in all; flag_off is the word offset of its key range's flags in the
+// exchange buffer.
 struct Segs {
   int n;
   int first_item[kMaxSegments + 1];
-  int n_rb[kMaxSegments], n_tiles[kMaxSegments];
+  int n_rb[kMaxSegments], n_tiles[kMaxSegments], n_main[kMaxSegments];
   int64_t q_lo[kMaxSegments], q_hi[kMaxSegments], k_lo[kMaxSegments], k_hi[kMaxSegments];
-  int64_t flag_off[kMaxSegments];
+  int64_t n_pre[kMaxSegments], flag_off[kMaxSegments];
 };
 
 // mbar_wait for warp-collective roles (softmax, RoPE): every lane waits and the
@@ -400,17 +404,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.k_lo = sg.k_lo[g];
     it.k_hi = sg.k_hi[g];
     it.n_tiles = sg.n_tiles[g];
+    it.n_main = sg.n_main[g];
+    it.n_pre = sg.n_pre[g];
     it.j0 = static_cast<int>((static_cast<int64_t>(rb) * it.n_tiles) / nrb);
     it.flags = share ? kflags + sg.flag_off[g] +
-                           (static_cast<int64_t>(it.b) * H + it.h) * it.n_tiles * 4
+                           (static_cast<int64_t>(it.b) * H + it.h) * it.n_main * 4
                      : nullptr;
     return it;
   };
   auto tile_at = [&](const Item &it, int j) {
     return it.j0 + j < it.n_tiles ? it.j0 + j : it.j0 + j - it.n_tiles;
   };
-  // first key row of tile tj of the item's key range
-  auto tile_row = [&](const Item &it, int tj) { return it.k_lo + static_cast<int64_t>(tj) * kBN; };
+  // first key row of tile tj of the item's key range: a row of K / V for the
+  // first n_main tiles, of the pre-rotated K / V after them
+  auto tile_row = [&](const Item &it, int tj) {
+    return tj < it.n_main ? it.k_lo + static_cast<int64_t>(tj) * kBN
+                          : static_cast<int64_t>(tj - it.n_main) * kBN;
+  };
+  // keys of tile tj that belong to the key range (the rest are masked)
+  auto tile_keys = [&](const Item &it, int tj) {
+    const int64_t kv = (tj < it.n_main ? it.k_hi : it.n_pre) - tile_row(it, tj);
+    return static_cast<int>(kv < kBN ? kv : kBN);
+  };
 
   if (tid == 0) {
     mbar_init(bar(kBarQRaw), 1);
@@ -539,7 +554,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // the acquire fence paid) before the ring wait, which hides both.
           // The first two tiles of a prepared item were rotated by this CTA's
           // RoPE warps, ordered before this point by the Q-prep wait.
-          bool rotated = share && k > 0 && j < 2;
+          // Pre-rotated tiles need no rotation at all.
+          const bool pre = tj >= it.n_main;
+          bool rotated = pre || (share && k > 0 && j < 2);
           if (share && !rotated) {
             const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
@@ -558,9 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // three arrivals are made here
             last_k_full |= 1u << s;
             last_k_par = (last_k_par & ~(1u << s)) | ((use & 1u) << s);
+            const CUtensorMap *src = pre ? &maps.kpre : &maps.krot;
             mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-            tma_load_4d(dst, &maps.krot, bar(kBarKFull + s), 0, h, krow, b);
-            tma_load_4d(dst + kBlockBytes, &maps.krot, bar(kBarKFull + s), 64, h, krow, b);
+            tma_load_4d(dst, src, bar(kBarKFull + s), 0, h, krow, b);
+            tma_load_4d(dst + kBlockBytes, src, bar(kBarKFull + s), 64, h, krow, b);
             mbar_arrive_n(bar(kBarKFull + s), 3);
           } else {
             const uint32_t par = (raw_par >> s) & 1u;
@@ -600,6 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 3 && lane == 0) {
       // ------------------------------------------------------ producer: V
       tma_prefetch_desc(&maps.v);
+      tma_prefetch_desc(&maps.vpre);
       int jt = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
@@ -607,19 +626,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = it.b, h = it.h, n_tiles = it.n_tiles;
         for (int j = 0; j < n_tiles; ++j, ++jt) {
           const int s = jt % kStages;
-          const int vrow = static_cast<int>(tile_row(it, tile_at(it, j)));
+          const int tj = tile_at(it, j);
+          const int vrow = static_cast<int>(tile_row(it, tj));
+          const CUtensorMap *src = tj < it.n_main ? &maps.v : &maps.vpre;
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           const uint32_t dst = sbase + kOffV + s * kTileBytes;
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
-          tma_load_4d(dst, &maps.v, bar(kBarVFull + s), 0, h, vrow, b);
-          tma_load_4d(dst + kBlockBytes, &maps.v, bar(kBarVFull + s), 64, h, vrow, b);
+          tma_load_4d(dst, src, bar(kBarVFull + s), 0, h, vrow, b);
+          tma_load_4d(dst + kBlockBytes, src, bar(kBarVFull + s), 64, h, vrow, b);
           // the tile two ahead into L2 now, so that its copy does not wait on
           // DRAM when the ring frees up
           if (j + kVPrefetch < n_tiles) {
-            const int prow = static_cast<int>(tile_row(it, tile_at(it, j + kVPrefetch)));
-            tma_prefetch_l2_4d(&maps.v, 0, h, prow, b);
-            tma_prefetch_l2_4d(&maps.v, 64, h, prow, b);
+            const int pj = tile_at(it, j + kVPrefetch);
+            const int prow = static_cast<int>(tile_row(it, pj));
+            const CUtensorMap *psrc = pj < it.n_main ? &maps.v : &maps.vpre;
+            tma_prefetch_l2_4d(psrc, 0, h, prow, b);
+            tma_prefetch_l2_4d(psrc, 64, h, prow, b);
           }
         }
       }
@@ -738,8 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN / 32; ++c)
           tmem_ld32_max(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]), mr[c]);
         tmem_ld_wait();
-        const int64_t kv = it.k_hi - tile_row(it, tile_at(it, j));  // keys of this tile in range
-        const int valid = static_cast<int>(kv < kBN ? kv : kBN);
+        const int valid = tile_keys(it, tile_at(it, j));
         float mx = fmax3(mr[0], mr[1], fmaxf(mr[2], mr[3]));
         if (valid < kBN) {
 #pragma unroll
@@ -911,8 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // from waiting long behind this work.
     auto prepare_piece = [&](int next, int c) {
       const Item nx = info(next);
-      const int kt = (c - 4) >> 1;  // K tile (0 or 1) of pieces 4-7
-      if (c < 4 || kt < nx.n_tiles) {
+      const int kt = (c - 4) >> 1;  // K tile (0 or 1) of pieces 4-7 (none if pre-rotated)
+      if (c < 4 || (kt < nx.n_tiles && tile_at(nx, kt) < nx.n_main)) {
         int64_t tok0, n_rows;
         const uint16_t *src;
         uint16_t *dst;
@@ -1114,7 +1136,8 @@ size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment 
 cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
                                       const uint32_t *table_q, const uint32_t *table_k,
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
-                                      const AttnSegment *segs, int n_segs, void *xbuf,
+                                      const AttnSegment *segs, int n_segs,
+                                      const PreRotatedKV *pre, void *xbuf,
                                       const QkNormArgs *norm, cudaStream_t stream) {
   if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
   static std::once_flag attr_once[64];
@@ -1138,6 +1161,17 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
       !make_head_map(&maps.v, v, B, S_k, H) || !make_head_map(&maps.out, out, B, S_q, H, 32, 32) ||
       !make_table_map(&maps.table_q, table_q, S_q) || !make_table_map(&maps.table_k, table_k, S_k))
     return cudaErrorInvalidValue;
+  const int64_t S_pre = pre != nullptr ? pre->S : 0;
+  if (S_pre < 0 || (S_pre > 0 && (pre->k == nullptr || pre->v == nullptr)))
+    return cudaErrorInvalidValue;
+  if (S_pre > 0) {
+    if (!make_head_map(&maps.kpre, pre->k, B, S_pre, H) ||
+        !make_head_map(&maps.vpre, pre->v, B, S_pre, H))
+      return cudaErrorInvalidValue;
+  } else {
+    maps.kpre = maps.k;  // never read
+    maps.vpre = maps.v;
+  }
   // segments, their items and their key ranges' flag offsets
   Segs sg{};
   sg.n = n_segs;
@@ -1156,7 +1190,7 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
   for (int g = 0; g < n_segs; ++g) {
     const AttnSegment &a = segs[g];
     if (a.q_lo < 0 || a.q_hi > S_q || a.k_lo < 0 || a.k_hi > S_k || a.k_hi <= a.k_lo ||
-        a.key_range < 0 || a.key_range >= kMaxSegments)
+        a.key_range < 0 || a.key_range >= kMaxSegments || a.n_pre < 0 || a.n_pre > S_pre)
       return cudaErrorInvalidValue;
     sg.first_item[g] = static_cast<int>(items);
     sg.q_lo[g] = a.q_lo;
@@ -1164,7 +1198,9 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     sg.k_lo[g] = a.k_lo;
     sg.k_hi[g] = a.k_hi;
     sg.n_rb[g] = static_cast<int>((a.q_hi - a.q_lo + kRowsPerCta - 1) / kRowsPerCta);
-    sg.n_tiles[g] = static_cast<int>((a.k_hi - a.k_lo + kBN - 1) / kBN);
+    sg.n_main[g] = static_cast<int>((a.k_hi - a.k_lo + kBN - 1) / kBN);
+    sg.n_pre[g] = a.n_pre;
+    sg.n_tiles[g] = sg.n_main[g] + static_cast<int>((a.n_pre + kBN - 1) / kBN);
     sg.flag_off[g] = range_off[a.key_range];
     items += static_cast<int64_t>(B) * H * (a.q_hi > a.q_lo ? sg.n_rb[g] : 0);
     if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
@@ -1214,9 +1250,9 @@ cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, 
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
                                    void *krot_scratch, const QkNormArgs *norm,
                                    cudaStream_t stream) {
-  const AttnSegment all{0, S, 0, S, 0};
+  const AttnSegment all{0, S, 0, S, 0, 0};
   return launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, &all, 1,
-                                   krot_scratch, norm, stream);
+                                   nullptr, krot_scratch, norm, stream);
 }
 
 }  // namespace flux

@@ -79,6 +79,14 @@ constexpr int kMaxSegments = 3;
 struct AttnSegment {
   int64_t q_lo, q_hi, k_lo, k_hi;
   int key_range;
+  int64_t n_pre;  // rows [0, n_pre) of the pre-rotated K / V join the key range
+};
+
+// Keys that arrive rotated already (a reference-image cache) and their
+// values: bf16 [B, S, H, 128]; they skip RoPE.
+struct PreRotatedKV {
+  const void *k, *v;
+  int64_t S;
 };
 
 // Bytes of the exchange buffer of launch_attention_segments: the flags of
@@ -94,7 +102,8 @@ size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment 
 cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
                                       const uint32_t *table_q, const uint32_t *table_k,
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
-                                      const AttnSegment *segs, int n_segs, void *xbuf,
+                                      const AttnSegment *segs, int n_segs,
+                                      const PreRotatedKV *pre, void *xbuf,
                                       const QkNormArgs *norm, cudaStream_t stream);
 
 // Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`

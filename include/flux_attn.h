@@ -263,13 +263,15 @@ int flux_joint_rope_attention_extract(const void *q, const void *k, const void *
  * flux_joint_rope_attention_cached: the cached mode. q, k, v, out are
  * [B, S_txt + S_img, H, D] for the tokens [txt ; img]; every query attends to
  * the keys [txt ; cached ref ; img] and the values in the same order. The
- * cached K is used as stored (already rotated, not rotated again).
+ * cached K is used as stored (already rotated, not rotated again); the
+ * kernel reads the cache in place, after the keys of k (the order of the
+ * keys does not change non-causal attention).
  *   cache_k, cache_v  device [B, S_ref, H, D] bf16, 16-byte aligned, as
- *                     written by flux_joint_rope_attention_extract.
+ *                     written by flux_joint_rope_attention_extract; NULL when
+ *                     S_ref is 0.
  *   workspace  >= flux_joint_rope_attention_cached_workspace(B, S_txt, S_img,
- *              S_ref, H, D) bytes, 256-byte aligned. It holds, besides the
- *              status word and tables, the keys and values gathered in the
- *              order [txt ; ref ; img].
+ *              S_ref, H, D) bytes, 256-byte aligned: the status word, the
+ *              table of [txt ; img] and the exchange buffer of rotated K / Q.
  * Other arguments and return codes as flux_joint_rope_attention.
  */
 size_t flux_joint_rope_attention_cached_workspace(int B, int64_t S_txt, int64_t S_img,
