@@ -6,7 +6,7 @@ Q/K tile loads, QK^T and PV on tcgen05, online softmax). FLOPs per step are
 4 * B * H * S^2 * 128.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload klein9b] [--qk-norm] [--kv-mode extract|cached]
+                    [--workload klein9b] [--qk-norm] [--kv-mode extract|cached] [--proj]
 
 Prints one JSON line (rank 0). With N > 1 (torchrun, one rank per GPU) every
 rank runs the same-shaped workload on its own seeded inputs with no data
@@ -15,7 +15,8 @@ all ranks' FLOPs over the slowest rank's time.
 
 `--kv-mode extract|cached` times one reference-image KV-mode call per step on
 the two-reference edit shape instead (tables, attention and, for extract, the
-cache copies inside the call).
+cache copies inside the call). `--proj` times the fused single-stream
+QKV + SwiGLU-MLP input projection of the workload (one GEMM kernel per step).
 
 `--impl reference` times the fp64 CPU oracle on the host cores instead, on a
 bounded sample of query rows of the same workload.
@@ -544,6 +545,164 @@ def run_kv(args, rank, world, local_rank):
     }
 
 
+# --------------------------------------------------------- single-stream projection
+
+
+def proj_cpu_baseline(w, target_s=10.0):
+    """The oracle's projection on a bounded sample of token rows (every output
+    feature of each row), timed on the host cores."""
+    import numpy as np
+
+    import oracle
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    M, dim, mlp = W.proj_dims(w)
+    x, wt = W.proj_inputs(w)
+    xn, wn = x.float().numpy().astype(np.float64), wt.float().numpy().astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.qkv_mlp_proj(xn, wn, w.H, 128, mlp, rows=np.array([0]))
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    n = int(max(2, min(M, target_s / per_row)))
+    rows = np.linspace(0, M - 1, n).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.qkv_mlp_proj(xn, wn, w.H, 128, mlp, rows=rows)
+    t = time.perf_counter() - t0
+    flops = 2 * rows.size * dim * (3 * dim + 2 * mlp)
+    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{rows.size} of {M} token rows x all {3 * dim + 2 * mlp} output features "
+                      f"of {w.name}, fp64, one thread, {t:.1f} s"}
+
+
+def run_proj(args, rank, world, local_rank):
+    """Time the fused single-stream input projection (one kernel per step)."""
+    import torch
+
+    from diffusion_transformer_joint_gb300 import binding
+    from diffusion_transformer_joint_gb300 import build as cuda_build
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(cuda_build.LIB_PATH):
+        cuda_build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+    w = W.WORKLOADS[args.workload]
+    M, dim, mlp = W.proj_dims(w)
+    H = w.H
+    x_h, wt_h = W.proj_inputs(w, seed_offset=rank_seed_offset(rank, 0))
+    wt = wt_h.to(dev)  # weights stay resident, as a model's do
+    set_bytes = x_h.numel() * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    xs = [x_h.to(dev)] + [W.proj_inputs(w, seed_offset=rank_seed_offset(rank, i))[0].to(dev)
+                          for i in range(1, n_sets)]
+    q = torch.empty((M, H, 128), dtype=torch.bfloat16, device=dev)
+    k, v = torch.empty_like(q), torch.empty_like(q)
+    act = torch.empty((M, mlp), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(i):
+        binding.qkv_mlp_proj(xs[i % n_sets], wt, H, mlp, q=q, k=k, v=v, act=act, status=status,
+                             stream=stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(K):
+                step(i)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    t_max = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+
+    # end to end: the activations from pinned host memory, the four outputs back
+    hx = x_h.pin_memory()
+    dx = torch.empty_like(hx, device=dev)
+    houts = [torch.empty_like(t, device="cpu").pin_memory() for t in (q, k, v, act)]
+
+    def e2e_one():
+        dx.copy_(hx, non_blocking=True)
+        binding.qkv_mlp_proj(dx, wt, H, mlp, q=q, k=k, v=v, act=act, status=status,
+                             stream=stream)
+        for h, d in zip(houts, (q, k, v, act)):
+            h.copy_(d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            e2e_one()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            e2e_one()
+        e1.record(stream)
+    stream.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError("device status set during the end-to-end steps")
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
+    if rank != 0:
+        return None
+    peaks, peak_src = _peaks()
+    flops = W.proj_flops(w)
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    ms = t_max / K
+    value = whole_job_tflops(flops, world, K, t_max)
+    achieved = flops / (ms * 1e-3) / 1e12
+    n_out = 3 * dim + 2 * mlp
+    line = {
+        "metric": f"fused single-stream QKV+MLP input projection bf16 TFLOP/s at the {w.name} shape",
+        "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,1/dim) bf16 weights)",
+        "config": {
+            "workload": f"{w.name} to_qkv_mlp_proj: M={M} tokens, dim={dim}, H={H}, "
+                        f"mlp={mlp}, W [{n_out}, {dim}]; epilogue split into Q/K/V "
+                        "[B,S,H,128] + SwiGLU",
+            "M": M, "dim": dim, "H": H, "mlp": mlp,
+            "parallelism": f"replicas x{world} (no collective)",
+            "l2": f"weights {wt.numel() * 2 / 2**20:.0f} MiB resident (> 129 MiB L2); "
+                  f"activations rotate over {n_sets} sets of {set_bytes / 2**20:.0f} MiB",
+            "step": "one fused projection kernel",
+        },
+        "roofline": {
+            "bound": "tensor", "kernel": "qkv_mlp_proj_kernel", "achieved": round(achieved, 2),
+            "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "frac_of_sustained": round(achieved / peak_sus, 4),
+            "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "algorithmic_bytes_per_launch": 2 * (M * dim + n_out * dim + M * (3 * dim + mlp)),
+        },
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(whole_job_tflops(flops, world, 1, e2e_ms), 2), "unit": UNIT,
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": hx.numel() * 2,
+                "d2h_bytes_per_step": sum(h.numel() * 2 for h in houts),
+                "api": "flux_qkv_mlp_proj (weights resident on the device)"},
+        "gpu_launches": K,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = proj_cpu_baseline(w, target_s=args.cpu_seconds)
+    return line
+
+
 # --------------------------------------------------------- CPU baseline
 
 
@@ -640,6 +799,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kv-mode", choices=("extract", "cached"), default=None,
                     help="time a reference-image KV-mode call on an edit workload instead")
+    ap.add_argument("--proj", action="store_true",
+                    help="time the fused single-stream QKV+MLP input projection instead")
     ap.add_argument("--qk-norm", action="store_true",
                     help="time the entry with the fused QK RMS normalisation before RoPE")
     args = ap.parse_args()
@@ -658,7 +819,9 @@ def main():
 
             torch.cuda.set_device(local_rank)
             dist.init_process_group("nccl")
-        if args.kv_mode is not None:
+        if args.proj:
+            line = run_proj(args, rank, world, local_rank)
+        elif args.kv_mode is not None:
             if args.workload == "klein9b":
                 args.workload = "klein9b_edit2"
             line = run_kv(args, rank, world, local_rank)

@@ -28,7 +28,7 @@ EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_atten
            "flux_joint_qknorm_rope_attention", "flux_joint_qknorm_rope_attention_tabled",
            "flux_joint_rope_attention_extract_workspace", "flux_joint_rope_attention_extract",
            "flux_joint_rope_attention_cached_workspace", "flux_joint_rope_attention_cached",
-           "flux_query_status", "flux_status_string")
+           "flux_qkv_mlp_proj", "flux_query_status", "flux_status_string")
 
 
 class FluxError(RuntimeError):
@@ -91,6 +91,8 @@ def load(path: str | None = None):
             lib.flux_joint_rope_attention_cached.argtypes = [
                 V, V, V, V, I64, V, I64, V, V, I64, I32, I32, I32, V, I32, D, V, V, SZ, V]
             lib.flux_joint_rope_attention_cached.restype = I32
+            lib.flux_qkv_mlp_proj.argtypes = [V, V, I64, I32, I32, I32, I64, V, V, V, V, V, V]
+            lib.flux_qkv_mlp_proj.restype = I32
             lib.flux_query_status.argtypes = [V, V]
             lib.flux_query_status.restype = I32
             lib.flux_status_string.argtypes = [I32]
@@ -369,6 +371,43 @@ def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES
     if rc != 0:
         raise FluxError("flux_joint_rope_attention_cached", rc, lib)
     return out
+
+
+def qkv_mlp_proj(x, w, H, mlp=None, q=None, k=None, v=None, act=None, status=None,
+                 stream=None):
+    """Fused single-stream input projection: x [..., dim] and w [3 H 128 + 2 mlp, dim]
+    bf16 -> (q, k, v [..., H, 128], act [..., mlp]); status (int32 [1], cleared
+    here when allocated) receives a device timeout."""
+    import torch
+
+    lib = load()
+    _need_cuda("x", x, torch.bfloat16)
+    _need_cuda("w", w, torch.bfloat16)
+    lead, dim = tuple(x.shape[:-1]), int(x.shape[-1])
+    M = 1
+    for n in lead:
+        M *= int(n)
+    inner = H * 128
+    if mlp is None:
+        mlp = (int(w.shape[0]) - 3 * inner) // 2
+    if tuple(w.shape) != (3 * inner + 2 * mlp, dim):
+        raise ValueError(f"w must be [{3 * inner + 2 * mlp}, {dim}], got {tuple(w.shape)}")
+    dev = x.device
+    q = torch.empty(lead + (H, 128), dtype=torch.bfloat16, device=dev) if q is None else q
+    k = torch.empty(lead + (H, 128), dtype=torch.bfloat16, device=dev) if k is None else k
+    v = torch.empty(lead + (H, 128), dtype=torch.bfloat16, device=dev) if v is None else v
+    if act is None:
+        act = torch.empty(lead + (mlp,), dtype=torch.bfloat16, device=dev)
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for name, t in (("q", q), ("k", k), ("v", v), ("act", act)):
+        _need_cuda(name, t, torch.bfloat16)
+    rc = lib.flux_qkv_mlp_proj(_ptr(x), _ptr(w), M, dim, int(H), 128, int(mlp), _ptr(q), _ptr(k),
+                               _ptr(v), _ptr(act) if mlp > 0 else None, _ptr(status),
+                               _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_qkv_mlp_proj", rc, lib)
+    return q, k, v, act
 
 
 def query_status(workspace, stream=None) -> int:

@@ -451,4 +451,40 @@ int flux_query_status(const void *workspace, void *stream) {
   return status;
 }
 
+int flux_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim, int H, int D,
+                      int64_t mlp_hidden, void *q, void *k, void *v, void *act, int32_t *status,
+                      void *stream) {
+  if (x == nullptr || w == nullptr || q == nullptr || k == nullptr || v == nullptr ||
+      status == nullptr || (mlp_hidden > 0 && act == nullptr))
+    return FLUX_ERR_NULL;
+  if (D != 128 || M < 1 || M > 0x7FFFFFFFLL || dim < 64 || dim % 64 != 0 || H < 1 ||
+      H > 65535 || mlp_hidden < 0 || mlp_hidden % 128 != 0 || mlp_hidden > 0x3FFFFFFFLL)
+    return FLUX_ERR_SHAPE;
+  const int64_t inner = static_cast<int64_t>(H) * D;
+  if (3 * inner + 2 * mlp_hidden > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      (mlp_hidden > 0 && !aligned16(act)))
+    return FLUX_ERR_ALIGN;
+  const size_t xb = static_cast<size_t>(M) * dim * 2;
+  const size_t wb = static_cast<size_t>(3 * inner + 2 * mlp_hidden) * dim * 2;
+  const size_t tb = static_cast<size_t>(M) * inner * 2;
+  const size_t ab = static_cast<size_t>(M) * mlp_hidden * 2;
+  const void *outs[4] = {q, k, v, act};
+  const size_t osz[4] = {tb, tb, tb, ab};
+  for (int i = 0; i < 4; ++i) {
+    if (osz[i] == 0) continue;
+    if (overlaps(outs[i], osz[i], x, xb) || overlaps(outs[i], osz[i], w, wb) ||
+        overlaps(outs[i], osz[i], status, sizeof(int32_t)))
+      return FLUX_ERR_ALIAS;
+    for (int j = i + 1; j < 4; ++j)
+      if (osz[j] > 0 && overlaps(outs[i], osz[i], outs[j], osz[j])) return FLUX_ERR_ALIAS;
+  }
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+  if (flux::launch_qkv_mlp_proj(x, w, M, dim, H, mlp_hidden, q, k, v, act, status,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return FLUX_OK;
+}
+
 }  // extern "C"

@@ -106,6 +106,17 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
                                       const PreRotatedKV *pre, void *xbuf,
                                       const QkNormArgs *norm, cudaStream_t stream);
 
+// The driver's cuTensorMapEncodeTiled, fetched once through the runtime (no
+// -lcuda); NULL when unavailable.
+void *tensor_map_encode_entry();
+
+// Enqueues the fused single-stream input projection: x [M, dim] and W
+// [3 * H * 128 + 2 * mlp, dim] bf16 row-major; q, k, v [M, H, 128] and act
+// [M, mlp] bf16 written. dim a multiple of 64, mlp a multiple of 128.
+cudaError_t launch_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim, int H,
+                                int64_t mlp, void *q, void *k, void *v, void *act, int *status,
+                                cudaStream_t stream);
+
 // Enqueues the attention kernel. q/k/v/out are [B, S, H, 128] bf16; `table`
 // is the packed table of the joint sequence; status is the device status word.
 // `krot_scratch` (256-byte aligned, krot_scratch_bytes long) lets the CTAs

@@ -110,6 +110,31 @@ def workload_qkv(w: Workload, seed_offset: int = 0):
             normal_bf16(shape, base + 3))
 
 
+MLP_RATIO = 3  # MLP width / hidden width of the FLUX.2 blocks
+
+
+def proj_dims(w: Workload):
+    """(M tokens, dim = hidden width = H * 128, mlp width) of the workload's
+    single-stream input projection."""
+    inner = w.H * w.D
+    return w.B * w.S, inner, MLP_RATIO * inner
+
+
+def proj_flops(w: Workload) -> int:
+    """2 * M * dim * (3 * inner + 2 * mlp): one multiply-add per weight and token."""
+    M, dim, mlp = proj_dims(w)
+    return 2 * M * dim * (3 * dim + 2 * mlp)
+
+
+def proj_inputs(w: Workload, seed_offset: int = 0):
+    """x [M, dim] ~ N(0, 1) and W [3 dim + 2 mlp, dim] ~ N(0, 1/dim) as bf16 CPU
+    tensors (synthetic activations and weights, seeds 1000*index + {11, 12})."""
+    M, dim, mlp = proj_dims(w)
+    base = 1000 * w.index + seed_offset
+    return (normal_bf16((M, dim), base + 11),
+            normal_bf16((3 * dim + 2 * mlp, dim), base + 12, scale=dim ** -0.5))
+
+
 def random_ids(S: int, seed: int, low: int = -600, high: int = 600, n_axes: int = 4):
     """Arbitrary int32 ids (any value is a valid position) for edge-case tests."""
     rng = np.random.default_rng(seed)

@@ -284,6 +284,35 @@ int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v
                                      void *out, void *workspace, size_t workspace_bytes,
                                      void *stream);
 
+/*
+ * flux_qkv_mlp_proj: the single-stream block's fused input projection
+ * ("Diffusers 中 Flux2Transformer2DModel 全面解析", sections 内部架构双流块与单流块:
+ * one linear layer, to_qkv_mlp_proj, yields Q, K, V and the MLP input; 激活函数与
+ * FFN: the SwiGLU gate is fused into it and the activation halves the width;
+ * 并行化支持: the packed MLP features are two equal halves, gate then linear).
+ * With y = x W^T (fp32 accumulation, no bias) and inner = H * D:
+ *   q = y[:, 0:inner], k = y[:, inner:2 inner], v = y[:, 2 inner:3 inner],
+ *   act = silu(y[:, 3 inner:3 inner + mlp]) * y[:, 3 inner + mlp:3 inner + 2 mlp],
+ * silu(g) = g / (1 + exp(-g)); every output rounded once to bf16 (nearest even).
+ *
+ *   x          device, bf16 [M, dim] row-major (M = B * S tokens), 16-byte aligned.
+ *   w          device, bf16 [3 * H * D + 2 * mlp_hidden, dim] row-major (a
+ *              linear layer's weight: one row per output feature), 16-byte aligned.
+ *   M          tokens, >= 1.  dim: a multiple of 64.  D == 128.
+ *   mlp_hidden MLP width (mlp_ratio * inner for FLUX.2), a multiple of 128; 0: none.
+ *   q, k, v    device, bf16 [M, H, D] each (= [B, S, H, D], the attention's
+ *              layout), 16-byte aligned; written, not read.
+ *   act        device, bf16 [M, mlp_hidden], 16-byte aligned; NULL when
+ *              mlp_hidden is 0.
+ *   status     device int32 word; the kernel writes FLUX_ERR_DEVICE_TIMEOUT
+ *              there if a bounded wait runs out and never writes it otherwise.
+ *   No output may overlap x, w, status or another output (FLUX_ERR_ALIAS).
+ * Returns FLUX_OK when the kernel was enqueued, else a negative status.
+ */
+int flux_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim, int H, int D,
+                      int64_t mlp_hidden, void *q, void *k, void *v, void *act, int32_t *status,
+                      void *stream);
+
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
  * on every device that loads this library, held until the process exits. */

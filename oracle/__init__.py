@@ -24,6 +24,9 @@ normalised attention with SDPA on inputs normalised and rotated separately.
 The reference KV modes agree with SDPA under an explicit boolean mask
 (extract) and over explicitly concatenated keys (cached), and a cache written
 in extract mode reproduces extract's text and image rows in cached mode.
+The fused single-stream projection places selected input channels exactly
+where the split puts them (Q, K, V heads, gate and linear halves), agrees with
+torch's float64 matmul and silu, and meets SiLU's closed forms.
 No function is "parity unpinned".
 """
 from __future__ import annotations
@@ -111,6 +114,10 @@ class Oracle:
             P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
             ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P, ctypes.c_int64, P]
         lib.oracle_attention_cached.restype = ctypes.c_int
+        lib.oracle_qkv_mlp_proj.argtypes = [
+            P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, P,
+            ctypes.c_int64, P, P, P, P]
+        lib.oracle_qkv_mlp_proj.restype = ctypes.c_int
         self.lib = lib
         self.path = lib_path
 
@@ -246,6 +253,30 @@ class Oracle:
         return out
 
 
+    def qkv_mlp_proj(self, x, w, H, D=128, mlp=None, rows=None):
+        """The single-stream fused projection for x [M, dim] and w [3HD + 2 mlp, dim]:
+        (q, k, v [n, H, D], act [n, mlp]) in fp64 for the rows (all M if None)."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        w = np.ascontiguousarray(w, dtype=np.float64)
+        M, dim = x.shape
+        inner = H * D
+        if mlp is None:
+            mlp = (w.shape[0] - 3 * inner) // 2
+        assert w.shape == (3 * inner + 2 * mlp, dim)
+        rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+        n = M if rows_arr is None else rows_arr.size
+        q = np.empty((n, H, D))
+        k = np.empty((n, H, D))
+        v = np.empty((n, H, D))
+        act = np.empty((n, mlp))
+        rc = self.lib.oracle_qkv_mlp_proj(_ptr(x), _ptr(w), M, dim, H, D, mlp,
+                                          None if rows_arr is None else _ptr(rows_arr), n,
+                                          _ptr(q), _ptr(k), _ptr(v), _ptr(act))
+        if rc != 0:
+            raise ValueError("oracle_qkv_mlp_proj: bad arguments")
+        return q, k, v, act
+
+
 def default() -> Oracle:
     global _default
     with _lock:
@@ -275,6 +306,10 @@ def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=(32,
                      theta=2000.0, rows=None):
     return default().attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims,
                                       theta, rows)
+
+
+def qkv_mlp_proj(x, w, H, D=128, mlp=None, rows=None):
+    return default().qkv_mlp_proj(x, w, H, D, mlp, rows)
 
 
 def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=(32, 32, 32, 32),

@@ -51,6 +51,22 @@
  *      is [txt, img] and the cached reference K / V are inserted between the
  *      text and the image keys and values).
  *
+ *   6. The single-stream block's fused input projection ("Diffusers 中
+ *      Flux2Transformer2DModel 全面解析", section "内部架构双流块与单流块": one
+ *      linear layer, to_qkv_mlp_proj, produces 3 * inner_dim + mlp_hidden_dim *
+ *      mlp_mult_factor features: the Q, K and V projections and the MLP's input
+ *      projection in one; section "激活函数与 FFN": the SwiGLU gate projection
+ *      is fused into the preceding linear layer and the activation halves the
+ *      width; section "并行化支持": that packed projection splits into two equal
+ *      halves, gate and linear). For a token row x[dim] and the weight
+ *      W[n_out, dim] (rows are output features):
+ *        y_n = sum_c W[n, c] x[c],  n < n_out = 3 * inner + 2 * mlp,
+ *        q = y[0, inner), k = y[inner, 2 inner), v = y[2 inner, 3 inner), each
+ *        read as [H, D] (inner = H * D, channel h * D + d is head h, dim d),
+ *        a_j = silu(y[3 inner + j]) * y[3 inner + mlp + j],  j < mlp,
+ *        silu(g) = g / (1 + exp(-g)).
+ *      No bias (the pages name none).
+ *
  * Layout: q, k, v, out are [B, S, H, D] row-major (D fastest), in double.
  * ids are [S, n_axes] int32 and are shared by every batch element.
  */
@@ -432,5 +448,42 @@ int oracle_attention_cached(const double *q, const double *k, const double *v, i
   free(vrows);
   free(cos_t);
   free(sin_t);
+  return 0;
+}
+
+/* Step 6: the fused Q / K / V / SwiGLU-MLP input projection of the single-stream
+ * block for the token rows `rows` (all M rows when rows is NULL). x [M, dim],
+ * w [3 * H * D + 2 * mlp, dim]; q, k, v [n, H, D] and act [n, mlp] for the n
+ * requested rows. Returns -1 on bad sizes. */
+static double proj_dot(const double *x, const double *w, int dim, int64_t n_out, int64_t n) {
+  double acc = 0.0;
+  const double *wn = w + n * dim; /* row n of W [n_out, dim] */
+  (void)n_out;
+  for (int c = 0; c < dim; ++c) acc += wn[c] * x[c];
+  return acc;
+}
+
+int oracle_qkv_mlp_proj(const double *x, const double *w, int64_t M, int dim, int H, int D,
+                        int64_t mlp, const int64_t *rows, int64_t n_rows, double *q, double *k,
+                        double *v, double *act) {
+  if (M < 0 || dim < 1 || H < 1 || D < 1 || mlp < 0) return -1;
+  const int64_t inner = (int64_t)H * D;
+  const int64_t n_out = 3 * inner + 2 * mlp;
+  const int64_t n = rows ? n_rows : M;
+  for (int64_t r = 0; r < n; ++r) {
+    const int64_t i = rows ? rows[r] : r;
+    if (i < 0 || i >= M) return -1;
+    const double *xi = x + i * dim;
+    for (int64_t c = 0; c < inner; ++c) {
+      q[r * inner + c] = proj_dot(xi, w, dim, n_out, c);
+      k[r * inner + c] = proj_dot(xi, w, dim, n_out, inner + c);
+      v[r * inner + c] = proj_dot(xi, w, dim, n_out, 2 * inner + c);
+    }
+    for (int64_t j = 0; j < mlp; ++j) {
+      const double g = proj_dot(xi, w, dim, n_out, 3 * inner + j);
+      const double u = proj_dot(xi, w, dim, n_out, 3 * inner + mlp + j);
+      act[r * mlp + j] = g / (1.0 + exp(-g)) * u;
+    }
+  }
   return 0;
 }

@@ -405,6 +405,81 @@ def check_extract_then_cached_reproduces_rows(orc):
     assert np.array_equal(sub2, out2[:, [2, 0]])
 
 
+def _torch_silu(x):
+    import torch
+
+    return torch.nn.functional.silu(torch.from_numpy(np.asarray(x, dtype=np.float64))).numpy()
+
+
+def check_proj_selection_weights(orc):
+    """Weights whose rows are unit vectors select input channels: every output
+    must be exactly the selected channel, placed where the split puts it
+    (Q, K, V heads in [H, D] order, then the gate and linear halves), and the
+    activation is torch's float64 silu of the gate times the linear half."""
+    rng = _rng(40)
+    M, dim, H, D, mlp = 5, 23, 3, 4, 7
+    inner = H * D
+    n_out = 3 * inner + 2 * mlp
+    pick = rng.integers(0, dim, size=n_out)
+    w = np.zeros((n_out, dim))
+    w[np.arange(n_out), pick] = 1.0
+    x = rng.standard_normal((M, dim))
+    q, k, v, act = orc.qkv_mlp_proj(x, w, H, D, mlp)
+    for t, base in ((q, 0), (k, inner), (v, 2 * inner)):
+        for h in range(H):
+            for d in range(D):
+                assert np.array_equal(t[:, h, d], x[:, pick[base + h * D + d]])
+    g = x[:, pick[3 * inner:3 * inner + mlp]]
+    u = x[:, pick[3 * inner + mlp:]]
+    assert np.allclose(act, _torch_silu(g) * u, rtol=1e-14, atol=1e-15)
+
+
+def check_proj_vs_torch_matmul(orc):
+    """Random weights: torch's float64 matmul and silu (library routines) on
+    slices taken by their column ranges."""
+    import torch
+
+    rng = _rng(41)
+    M, dim, H, D, mlp = 9, 64, 2, 8, 24
+    inner = H * D
+    x = rng.standard_normal((M, dim))
+    w = rng.standard_normal((3 * inner + 2 * mlp, dim)) / math.sqrt(dim)
+    y = (torch.from_numpy(x) @ torch.from_numpy(w).T).numpy()
+    q, k, v, act = orc.qkv_mlp_proj(x, w, H, D, mlp)
+    assert np.allclose(q.reshape(M, inner), y[:, :inner], rtol=1e-12, atol=1e-13)
+    assert np.allclose(k.reshape(M, inner), y[:, inner:2 * inner], rtol=1e-12, atol=1e-13)
+    assert np.allclose(v.reshape(M, inner), y[:, 2 * inner:3 * inner], rtol=1e-12, atol=1e-13)
+    g, u = y[:, 3 * inner:3 * inner + mlp], y[:, 3 * inner + mlp:]
+    assert np.allclose(act, _torch_silu(g) * u, rtol=1e-12, atol=1e-13)
+    rows = np.array([M - 1, 0, 4])
+    sq, sk, sv, sa = orc.qkv_mlp_proj(x, w, H, D, mlp, rows=rows)
+    assert np.array_equal(sq, q[rows]) and np.array_equal(sa, act[rows])
+    assert np.array_equal(sk, k[rows]) and np.array_equal(sv, v[rows])
+
+
+def check_proj_silu_closed_forms(orc):
+    """SiLU's closed forms through the projection: silu(0) = 0,
+    silu(g) - silu(-g) = g, silu(g) -> g for large g and -> 0 for very
+    negative g (a linear half of ones makes act = silu(gate))."""
+    rng = _rng(42)
+    H, D, mlp, dim = 1, 2, 6, 3
+    inner = H * D
+    w = np.zeros((3 * inner + 2 * mlp, dim))
+    w[3 * inner:3 * inner + mlp, 0] = [0.0, 1.0, -1.0, 2.5, -2.5, 1.0]
+    w[3 * inner + mlp:, 1] = 1.0  # the linear half reads channel 1
+    for g0 in (0.7, -1.3, 3.1):
+        x = np.array([[g0, 1.0, rng.standard_normal()]])
+        _, _, _, a = orc.qkv_mlp_proj(x, w, H, D, mlp)
+        a = a[0]
+        assert a[0] == 0.0
+        assert abs((a[1] - a[2]) - g0) < 1e-15
+        assert abs((a[3] - a[4]) - 2.5 * g0) < 1e-14
+        assert abs(a[5] - g0 / (1.0 + math.exp(-g0))) < 1e-15
+    x = np.array([[60.0, 1.0, 0.0]])
+    _, _, _, a = orc.qkv_mlp_proj(x, w, H, D, mlp)
+    assert abs(a[0, 1] - 60.0) < 1e-12 and abs(a[0, 2]) < 1e-20
+
+
 ALL_CHECKS = [
     check_zero_ids_identity,
     check_frequencies_high_precision,
@@ -426,4 +501,7 @@ ALL_CHECKS = [
     check_extract_mode_vs_masked_sdpa,
     check_cached_mode_vs_concatenated_sdpa,
     check_extract_then_cached_reproduces_rows,
+    check_proj_selection_weights,
+    check_proj_vs_torch_matmul,
+    check_proj_silu_closed_forms,
 ]

@@ -190,3 +190,27 @@ def test_kv_mode_workspace_sizes_and_checks(lib):
         P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(2048), 32, P(300 * 1024),
         P(200 * 1024 + 8), 8, 1, 2, 128, axes, 4, 2000.0, P(48 * 1024 * 1024), P(256 * 65536),
         cneed, None) == -4
+
+
+def test_qkv_mlp_proj_argument_checks(lib):
+    P = ctypes.c_void_p
+    MB = 1 << 20
+
+    def call(x=16, w=64 * MB, M=100, dim=128, H=2, D=128, mlp=256, q=128 * MB, k=129 * MB,
+             v=130 * MB, act=131 * MB, status=200 * MB):
+        return lib.flux_qkv_mlp_proj(P(x) if x else None, P(w) if w else None, M, dim, H, D, mlp,
+                                     P(q) if q else None, P(k) if k else None,
+                                     P(v) if v else None, P(act) if act else None,
+                                     P(status) if status else None, None)
+
+    assert call(x=0) == -1
+    assert call(status=0) == -1
+    assert call(act=0) == -1               # the MLP half needs act
+    assert call(D=64) == -2
+    assert call(dim=96) == -2              # dim a multiple of 64
+    assert call(mlp=200) == -2             # mlp a multiple of 128
+    assert call(M=0) == -2
+    assert call(q=128 * MB + 8) == -4
+    assert call(k=128 * MB + 4096) == -9   # k overlaps q
+    assert call(act=1024) == -9            # act overlaps x
+    assert call(v=64 * MB + 64) == -9      # v overlaps w

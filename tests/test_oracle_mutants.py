@@ -78,6 +78,19 @@ MUTANTS = {
     # off-by-one in the key loop
     "skip_last_key": ("for (int64_t j = 0; j < S; ++j) {\n      double acc",
                       "for (int64_t j = 0; j < S - 1; ++j) {\n      double acc"),
+    "proj_gate_linear_swapped": ("proj_dot(xi, w, dim, n_out, 3 * inner + j);",
+                                 "proj_dot(xi, w, dim, n_out, 3 * inner + mlp + j);"),
+    "proj_no_sigmoid": ("act[r * mlp + j] = g / (1.0 + exp(-g)) * u;",
+                        "act[r * mlp + j] = g * u;"),
+    "proj_sigmoid_sign": ("act[r * mlp + j] = g / (1.0 + exp(-g)) * u;",
+                          "act[r * mlp + j] = g / (1.0 + exp(g)) * u;"),
+    "proj_k_from_q": ("proj_dot(xi, w, dim, n_out, inner + c);",
+                      "proj_dot(xi, w, dim, n_out, c);"),
+    "proj_v_from_k": ("proj_dot(xi, w, dim, n_out, 2 * inner + c);",
+                      "proj_dot(xi, w, dim, n_out, inner + c);"),
+    "proj_weight_transposed": ("acc += wn[c] * x[c];", "acc += w[(int64_t)c * n_out + n] * x[c];"),
+    "proj_last_channel_skipped": ("for (int c = 0; c < dim; ++c) acc += wn[c]",
+                                  "for (int c = 0; c < dim - 1; ++c) acc += wn[c]"),
 }
 
 

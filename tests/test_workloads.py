@@ -34,6 +34,18 @@ def test_workloads_match_printed_config():
     assert e.S == 512 + 3 * 4096 == 12800 and e.H == 32
 
 
+def test_projection_dims_match_printed_config():
+    g = _golden()
+    for name in ("klein4b", "klein9b", "dev32b"):
+        w = W.WORKLOADS[name]
+        M, dim, mlp = W.proj_dims(w)
+        assert dim == g["hidden_" + name][0] and M == w.S
+        assert 10 * mlp == g["mlp_ratio_tenths"][0] * dim
+        assert W.proj_flops(w) == 2 * M * dim * (3 * dim + g["mlp_halves"][0] * mlp)
+    x, wt = W.proj_inputs(W.WORKLOADS["tiny"])
+    assert tuple(x.shape) == (80, 256) and tuple(wt.shape) == (3 * 256 + 2 * 768, 256)
+
+
 def test_ids_recipe():
     w = W.WORKLOADS["klein9b_edit2"]
     txt, img = W.workload_ids(w)
