@@ -43,6 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attention_klein9b_ncu.txt")
 KERNEL_SOURCE = os.path.join(ROOT, "diffusion_transformer_joint_gb300", "csrc",
                              "attention_sm103a.cu")
+PROJ_PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "qkv_mlp_proj_ncu.txt")
+PROJ_SOURCE = os.path.join(ROOT, "diffusion_transformer_joint_gb300", "csrc", "proj_sm103a.cu")
 
 
 def _peaks():
@@ -55,23 +57,24 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _kernel_hash():
-    with open(KERNEL_SOURCE, "rb") as f:
+def _kernel_hash(source=KERNEL_SOURCE):
+    with open(source, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def _profiled_traffic():
-    """dram bytes per attention launch from the committed ncu summary, when
-    it was taken on the current kernel source; else None."""
+def _profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE,
+                      key="dram_bytes_per_launch_klein9b"):
+    """dram bytes per launch from a committed ncu summary, when it was taken
+    on the current kernel source; else None."""
     try:
         vals = {}
-        for line in open(PROFILE_SUMMARY):
+        for line in open(summary):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 vals[k.strip()] = v.strip()
-        if vals.get("kernel_source_sha256_16") != _kernel_hash():
+        if vals.get("kernel_source_sha256_16") != _kernel_hash(source):
             return None
-        return float(vals["dram_bytes_per_launch_klein9b"])
+        return float(vals[key])
     except (OSError, KeyError, ValueError):
         return None
 
@@ -687,7 +690,9 @@ def run_proj(args, rank, world, local_rank):
             "bound": "tensor", "kernel": "qkv_mlp_proj_kernel", "achieved": round(achieved, 2),
             "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
             "frac_of_sustained": round(achieved / peak_sus, 4),
-            "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+            "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "traffic": _profiled_traffic(PROJ_PROFILE_SUMMARY, PROJ_SOURCE,
+                                         f"dram_bytes_per_launch_{w.name}"),
             "algorithmic_flops_per_launch": flops,
             "algorithmic_bytes_per_launch": 2 * (M * dim + n_out * dim + M * (3 * dim + mlp)),
         },

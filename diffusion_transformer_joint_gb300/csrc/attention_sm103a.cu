@@ -1100,8 +1100,6 @@ bool make_table_map(CUtensorMap *map, const uint32_t *table, int64_t S) {
 
 }  // namespace
 
-void *tensor_map_encode_entry() { return reinterpret_cast<void *>(encode_fn()); }
-
 // A value no earlier launch in this process used, for the exchange flags: a
 // flag equal to it was written during this launch. The counter is mixed
 // (splitmix64 finaliser) with a per-process salt so that stale flag words

@@ -106,8 +106,8 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
                                       const PreRotatedKV *pre, void *xbuf,
                                       const QkNormArgs *norm, cudaStream_t stream);
 
-// The driver's cuTensorMapEncodeTiled, fetched once through the runtime (no
-// -lcuda); NULL when unavailable.
+// The driver's cuTensorMapEncodeTiled for the projection's tensor maps,
+// fetched once through the runtime (no -lcuda); NULL when unavailable.
 void *tensor_map_encode_entry();
 
 // Enqueues the fused single-stream input projection: x [M, dim] and W

@@ -307,6 +307,21 @@ bool make_rows_map(CUtensorMap *map, const void *x, int64_t rows, int64_t cols) 
 
 }  // namespace
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+void *tensor_map_encode_entry() {
+  static void *fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = p;
+  });
+  return fn;
+}
+
 cudaError_t launch_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim, int H,
                                 int64_t mlp, void *q, void *k, void *v, void *act, int *status,
                                 cudaStream_t stream) {
