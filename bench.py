@@ -303,13 +303,37 @@ def run_ours(args, rank, world, local_rank):
                 "unit": UNIT, "ms_per_step": round(e2e["ms_per_step"], 4),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                 "api": "flux_joint_rope_attention (one call: tables + attention)",
-                "pipelining": "two streams with their own buffers: a step's host-to-device "
-                              "copies overlap the previous step's kernels and copy back"},
+                "pipelining": PIPELINING},
         "gpu_launches": 2 * K,
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
     return line
+
+
+PIPELINING = ("two streams with their own buffers: a step's host-to-device copies overlap "
+              "the previous step's kernels and copy back")
+
+
+def two_lane_ms(torch, dev, K, warmup, lanes, one):
+    """ms per step of one(i, lane) run for i < K, alternating between two lanes
+    (dicts with their own "stream" and buffers): a step's copies overlap the
+    other lane's kernels; within a lane the steps stay in order."""
+    for i in range(max(2, warmup)):
+        one(i, lanes[i % 2])
+    torch.cuda.synchronize(dev)
+    main = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for ln in lanes:
+        ln["stream"].wait_event(e0)
+    for i in range(K):
+        one(i, lanes[i % 2])
+    for ln in lanes:
+        main.wait_stream(ln["stream"])
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    return e0.elapsed_time(e1) / K
 
 
 def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
@@ -335,8 +359,7 @@ def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
         lane["out"] = torch.empty_like(lane["in"][0])
         lanes.append(lane)
 
-    def one(i):
-        ln = lanes[i % 2]
+    def one(i, ln):
         st = ln["stream"]
         with torch.cuda.stream(st):
             for d, h in zip(ln["in"], (hq, hk, hv, htxt, himg)):
@@ -346,26 +369,13 @@ def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
                                          workspace=ln["ws"], stream=st)
             ln["hout"].copy_(ln["out"], non_blocking=True)
 
-    for i in range(max(2, warmup)):
-        one(i)
-    torch.cuda.synchronize(dev)
-    main = torch.cuda.current_stream(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(main)
-    for ln in lanes:
-        ln["stream"].wait_event(e0)
-    for i in range(K):
-        one(i)
-    for ln in lanes:
-        main.wait_stream(ln["stream"])
-    e1.record(main)
-    torch.cuda.synchronize(dev)
+    ms = two_lane_ms(torch, dev, K, warmup, lanes, one)
     for ln in lanes:
         if binding.query_status(ln["ws"], ln["stream"]) != 0:
             raise RuntimeError("device status set during the end-to-end steps")
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, htxt, himg))
     d2h = lanes[0]["hout"].numel() * lanes[0]["hout"].element_size()
-    return {"ms_per_step": e0.elapsed_time(e1) / K, "h2d": h2d, "d2h": d2h}
+    return {"ms_per_step": ms, "h2d": h2d, "d2h": d2h}
 
 
 # --------------------------------------------------------- reference-image KV modes
@@ -488,37 +498,39 @@ def run_kv(args, rank, world, local_rank):
     # end to end: pinned host inputs in, the call, the outputs (and cache) back
     h_in = tuple(t.pin_memory() for t in tensors0)
     h_ids = tuple(torch.from_numpy(np.ascontiguousarray(x)).pin_memory() for x in ids_h)
-    d_in = tuple(torch.empty_like(t, device=dev) for t in h_in)
-    d_ids = tuple(torch.empty_like(t, device=dev) for t in h_ids)
-    d_out = sets[0][1]
-    h_out = tuple(torch.empty_like(t, device="cpu").pin_memory() for t in d_out)
+    lanes = []
+    for li in range(2):
+        lanes.append({
+            "in": tuple(torch.empty_like(t, device=dev) for t in h_in),
+            "ids": tuple(torch.empty_like(t, device=dev) for t in h_ids),
+            "out": tuple(torch.empty_like(t) for t in sets[0][1]),
+            "hout": tuple(torch.empty_like(t, device="cpu").pin_memory() for t in sets[0][1]),
+            "ws": ws if li == 0 else torch.zeros_like(ws),
+            "stream": stream if li == 0 else torch.cuda.Stream(device=dev),
+        })
 
-    def e2e_one():
-        for d, h in zip(d_in + d_ids, h_in + h_ids):
-            d.copy_(h, non_blocking=True)
-        if mode == "extract":
-            binding.attention_extract(*d_in, *d_ids, out=d_out[0], cache_k=d_out[1],
-                                      cache_v=d_out[2], workspace=ws, stream=stream)
-        else:
-            q, k, v, ck, cv = d_in
-            binding.attention_cached(q, k, v, d_ids[0], d_ids[1], ck, cv, out=d_out[0],
-                                     workspace=ws, stream=stream)
-        for h, d in zip(h_out, d_out):
-            h.copy_(d, non_blocking=True)
+    def e2e_one(i, ln):
+        st = ln["stream"]
+        with torch.cuda.stream(st):
+            for d, h in zip(ln["in"] + ln["ids"], h_in + h_ids):
+                d.copy_(h, non_blocking=True)
+            d_in, d_ids, d_out = ln["in"], ln["ids"], ln["out"]
+            if mode == "extract":
+                binding.attention_extract(*d_in, *d_ids, out=d_out[0], cache_k=d_out[1],
+                                          cache_v=d_out[2], workspace=ln["ws"], stream=st)
+            else:
+                q, k, v, ck, cv = d_in
+                binding.attention_cached(q, k, v, d_ids[0], d_ids[1], ck, cv, out=d_out[0],
+                                         workspace=ln["ws"], stream=st)
+            for h, d in zip(ln["hout"], d_out):
+                h.copy_(d, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_one()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            e2e_one()
-        e1.record(stream)
-    stream.synchronize()
-    if binding.query_status(ws, stream) != 0:
-        raise RuntimeError("device status set during the end-to-end steps")
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
+    e2e_step_ms = two_lane_ms(torch, dev, K, args.warmup, lanes, e2e_one)
+    for ln in lanes:
+        if binding.query_status(ln["ws"], ln["stream"]) != 0:
+            raise RuntimeError("device status set during the end-to-end steps")
+    h_out = lanes[0]["hout"]
+    e2e_ms = max_over_ranks(e2e_step_ms, dist, dev)
     if rank != 0:
         return None
 
@@ -560,7 +572,7 @@ def run_kv(args, rank, world, local_rank):
                 "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in h_in + h_ids),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in h_out),
-                "api": f"flux_joint_rope_attention_{mode}"},
+                "api": f"flux_joint_rope_attention_{mode}", "pipelining": PIPELINING},
         "gpu_launches": (3 if mode == "extract" else 2) * K,
     }
 
@@ -654,29 +666,31 @@ def run_proj(args, rank, world, local_rank):
 
     # end to end: the activations from pinned host memory, the four outputs back
     hx = x_h.pin_memory()
-    dx = torch.empty_like(hx, device=dev)
-    houts = [torch.empty_like(t, device="cpu").pin_memory() for t in (q, k, v, act)]
+    lanes = []
+    for li in range(2):
+        outs = (q, k, v, act) if li == 0 else tuple(torch.empty_like(t) for t in (q, k, v, act))
+        lanes.append({
+            "x": torch.empty_like(hx, device=dev), "out": outs,
+            "hout": tuple(torch.empty_like(t, device="cpu").pin_memory() for t in outs),
+            "status": torch.zeros(1, dtype=torch.int32, device=dev),
+            "stream": stream if li == 0 else torch.cuda.Stream(device=dev),
+        })
 
-    def e2e_one():
-        dx.copy_(hx, non_blocking=True)
-        binding.qkv_mlp_proj(dx, wt, H, mlp, q=q, k=k, v=v, act=act, status=status,
-                             stream=stream)
-        for h, d in zip(houts, (q, k, v, act)):
-            h.copy_(d, non_blocking=True)
+    def e2e_one(i, ln):
+        st = ln["stream"]
+        with torch.cuda.stream(st):
+            ln["x"].copy_(hx, non_blocking=True)
+            oq, ok_, ov, oa = ln["out"]
+            binding.qkv_mlp_proj(ln["x"], wt, H, mlp, q=oq, k=ok_, v=ov, act=oa,
+                                 status=ln["status"], stream=st)
+            for h, d in zip(ln["hout"], ln["out"]):
+                h.copy_(d, non_blocking=True)
 
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            e2e_one()
-        stream.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(K):
-            e2e_one()
-        e1.record(stream)
-    stream.synchronize()
-    if int(status.item()) != 0:
+    e2e_step_ms = two_lane_ms(torch, dev, K, args.warmup, lanes, e2e_one)
+    if any(int(ln["status"].item()) != 0 for ln in lanes):
         raise RuntimeError("device status set during the end-to-end steps")
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / K, dist, dev)
+    houts = lanes[0]["hout"]
+    e2e_ms = max_over_ranks(e2e_step_ms, dist, dev)
     if rank != 0:
         return None
     peaks, peak_src = _peaks()
@@ -717,7 +731,8 @@ def run_proj(args, rank, world, local_rank):
         "e2e": {"value": round(whole_job_tflops(flops, world, 1, e2e_ms), 2), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": hx.numel() * 2,
                 "d2h_bytes_per_step": sum(h.numel() * 2 for h in houts),
-                "api": "flux_qkv_mlp_proj (weights resident on the device)"},
+                "api": "flux_qkv_mlp_proj (weights resident on the device)",
+                "pipelining": PIPELINING},
         "gpu_launches": K,
     }
     if not args.no_cpu_baseline:
