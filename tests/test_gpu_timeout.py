@@ -79,3 +79,59 @@ def test_bounded_wait_reports_timeout_and_context_survives(tmp_path):
     ref = oracle.joint_rope_attention(q.float().cpu().numpy(), k.float().cpu().numpy(),
                                       v.float().cpu().numpy(), txt_np, img_np)
     assert np.abs(good.float().cpu().numpy() - ref).max() <= 1e-2
+
+
+PROJ_ANCHOR = "if (lane == 0) mbar_arrive(bar(kBarAccEmpty + buf));"
+PROJ_WITHHELD = "if (lane == 0 && lt != 0) mbar_arrive(bar(kBarAccEmpty + buf));"
+
+
+def test_projection_bounded_wait_reports_timeout(tmp_path):
+    """The fused projection's epilogue warps withhold the release of their
+    first accumulator; a CTA with a third tile then waits for it in its MMA
+    warp until the bounded wait runs out. 320 tiles over at most 152 CTAs
+    give CTA 0 a third tile."""
+    build.build()
+    binding.load()
+    src = tmp_path / "csrc"
+    shutil.copytree(build.CSRC, src)
+    f = src / "proj_sm103a.cu"
+    text = f.read_text()
+    assert text.count(PROJ_ANCHOR) == 1, "the accumulator release was not found exactly once"
+    f.write_text(text.replace(PROJ_ANCHOR, PROJ_WITHHELD))
+    out = tmp_path / "libflux_proj_withheld.so"
+    flags = [x for x in build.NVCC_FLAGS if x not in ("-Xptxas", "-v")]
+    subprocess.run([build.nvcc(), *flags, "-I", build.INCLUDE, "-I", str(src),
+                    *sorted(str(p) for p in src.glob("*.cu")), "-o", str(out)],
+                   check=True, capture_output=True)
+    lib = ctypes.CDLL(str(out))
+    V, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.flux_qkv_mlp_proj.argtypes = [V, V, I64, I32, I32, I32, I64, V, V, V, V, V, V]
+    lib.flux_qkv_mlp_proj.restype = I32
+    M, dim, H, mlp = 1280, 64, 16, 1024  # 10 row blocks x (24 + 8) feature tiles
+    x = W.normal_bf16((M, dim), 31).cuda()
+    w = W.normal_bf16((3 * H * 128 + 2 * mlp, dim), 32, scale=dim ** -0.5).cuda()
+    q, k, v = (torch.empty((M, H, 128), dtype=torch.bfloat16, device="cuda") for _ in range(3))
+    act = torch.empty((M, mlp), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+    P = lambda t: ctypes.c_void_p(t.data_ptr())
+    t0 = time.time()
+    rc = lib.flux_qkv_mlp_proj(P(x), P(w), M, dim, H, 128, mlp, P(q), P(k), P(v), P(act),
+                               P(status), ctypes.c_void_p(stream.cuda_stream))
+    assert rc == 0
+    torch.cuda.synchronize()
+    elapsed = time.time() - t0
+    assert int(status.item()) == -7, f"expected FLUX_ERR_DEVICE_TIMEOUT, got {int(status.item())}"
+    assert elapsed < 60.0, f"bounded wait took {elapsed:.1f} s"
+    # the context is usable: the regular library runs and is correct
+    status.zero_()
+    gq, _, _, gact = binding.qkv_mlp_proj(x, w, H, mlp, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rows = np.array([0, 700, M - 1])
+    rq, _, _, ra = oracle.qkv_mlp_proj(x.float().cpu().numpy(), w.float().cpu().numpy(), H, 128,
+                                       mlp, rows=rows)
+    gq_np = gq.float().cpu().numpy()[rows]
+    assert np.all(np.abs(gq_np - rq) <= 2.0 ** -8 * np.abs(rq) + 1e-4)
+    ga_np = gact.float().cpu().numpy()[rows]
+    assert np.all(np.abs(ga_np - ra) <= 2.0 ** -8 * np.abs(ra) + 1e-4)
