@@ -260,3 +260,17 @@ def test_full_workload_sampled_rows(name):
     # every output finite and bounded by the largest |v| (a convex combination)
     assert torch.isfinite(out).all()
     assert out.abs().max().item() <= v.abs().max().item() + 1e-2
+
+
+@pytest.mark.parametrize("B,H,S", [(1, 160, 256), (1, 9, 4352), (2, 80, 300)])
+def test_more_items_than_blocks_all_outputs(B, H, S):
+    """More work items (batch, head, 256-row block) than thread blocks, with a
+    last partial wave (160, 153 and 320 items): every output against the
+    oracle."""
+    q = W.normal_bf16((B, S, H, 128), 91 + S)
+    k = W.normal_bf16((B, S, H, 128), 92 + S)
+    v = W.normal_bf16((B, S, H, 128), 93 + S)
+    ids = W.random_ids(S, 94 + S, 0, 300)
+    txt, img = ids[:40], ids[40:]
+    out = _run_gpu(q, k, v, txt, img)
+    _compare(out, q, k, v, txt, img)
