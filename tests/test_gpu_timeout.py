@@ -81,15 +81,16 @@ def test_bounded_wait_reports_timeout_and_context_survives(tmp_path):
     assert np.abs(good.float().cpu().numpy() - ref).max() <= 1e-2
 
 
-PROJ_ANCHOR = "if (lane == 0) mbar_arrive(bar(kBarAccEmpty + buf));"
-PROJ_WITHHELD = "if (lane == 0 && lt != 0) mbar_arrive(bar(kBarAccEmpty + buf));"
+PROJ_ANCHOR = "if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * static_cast<uint32_t>(buf));"
+PROJ_WITHHELD = ("if (lane == 0 && lt != 0) "
+                 "mbar_arrive_cluster(acc_empty0 + 8u * static_cast<uint32_t>(buf));")
 
 
 def test_projection_bounded_wait_reports_timeout(tmp_path):
     """The fused projection's epilogue warps withhold the release of their
-    first accumulator; a CTA with a third tile then waits for it in its MMA
-    warp until the bounded wait runs out. 320 tiles over at most 152 CTAs
-    give CTA 0 a third tile."""
+    first accumulator; a CTA pair with a third tile then waits for it in its
+    MMA warp until the bounded wait runs out. 160 tiles over at most 76 CTA
+    pairs give pair 0 a third tile."""
     build.build()
     binding.load()
     src = tmp_path / "csrc"
@@ -107,7 +108,7 @@ def test_projection_bounded_wait_reports_timeout(tmp_path):
     V, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.flux_qkv_mlp_proj.argtypes = [V, V, I64, I32, I32, I32, I64, V, V, V, V, V, V]
     lib.flux_qkv_mlp_proj.restype = I32
-    M, dim, H, mlp = 1280, 64, 16, 1024  # 10 row blocks x (24 + 8) feature tiles
+    M, dim, H, mlp = 1280, 64, 16, 1024  # 5 256-row blocks x (24 + 8) feature tiles
     x = W.normal_bf16((M, dim), 31).cuda()
     w = W.normal_bf16((3 * H * 128 + 2 * mlp, dim), 32, scale=dim ** -0.5).cuda()
     q, k, v = (torch.empty((M, H, 128), dtype=torch.bfloat16, device="cuda") for _ in range(3))
