@@ -569,6 +569,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
+          if (share && !rotated) {
+            // A second look once the ring slot is free: decided early, the
+            // first look misses tiles the CTAs that started the head at the
+            // same time publish while this one waits (the first item's tiles
+            // after its own two).
+            const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
+            uint64_t f0, f1, f2, f3;
+            ld_relaxed_gpu_v2_u64(fl, f0, f1);
+            ld_relaxed_gpu_v2_u64(fl + 2, f2, f3);
+            rotated = f0 == token && f1 == token && f2 == token && f3 == token;
+            if (rotated) {
+              fence_acq_rel_gpu();
+              fence_proxy_async_global();
+            }
+          }
           const uint32_t dst = sbase + kOffK + s * kTileBytes;
           if (rotated) {
             // straight to the MMA: the copy completes K-full, whose other
