@@ -2,6 +2,7 @@
 // workspace layout, and the two launches (RoPE tables, then attention).
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstring>
 
 #include "flux_internal.h"
@@ -17,18 +18,20 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
 
 // sm_103 check, cached per device ordinal.
 int check_device() {
-  static int cached[64];  // 0 unknown, 1 ok, -1 unsupported
+  static std::atomic<int> cached[64];  // 0 unknown, 1 ok, -1 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLUX_ERR_CUDA;
   if (dev < 0 || dev >= 64) return FLUX_ERR_UNSUPPORTED;
-  if (cached[dev] == 0) {
+  int c = cached[dev].load(std::memory_order_relaxed);
+  if (c == 0) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return FLUX_ERR_CUDA;
-    cached[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    c = (major == 10 && minor == 3) ? 1 : -1;
+    cached[dev].store(c, std::memory_order_relaxed);
   }
-  return cached[dev] == 1 ? FLUX_OK : FLUX_ERR_UNSUPPORTED;
+  return c == 1 ? FLUX_OK : FLUX_ERR_UNSUPPORTED;
 }
 
 }  // namespace

@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -410,16 +411,16 @@ cudaError_t launch_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // persistent: as many pairs as can be resident at once, no more than tiles
-  static int max_pairs[64];
-  if (max_pairs[dev] == 0) {
-    int n = 0;
+  static std::atomic<int> max_pairs[64];
+  int np = max_pairs[dev].load(std::memory_order_relaxed);
+  if (np == 0) {
     cfg.gridDim = dim3(2, 1, 1);
-    e = cudaOccupancyMaxActiveClusters(&n, qkv_mlp_proj_kernel, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&np, qkv_mlp_proj_kernel, &cfg);
     if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_pairs[dev] = n;
+    if (np < 1) return cudaErrorInvalidConfiguration;
+    max_pairs[dev].store(np, std::memory_order_relaxed);
   }
-  const int64_t pairs = n_tiles < max_pairs[dev] ? n_tiles : max_pairs[dev];
+  const int64_t pairs = n_tiles < np ? n_tiles : np;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
   return cudaLaunchKernelEx(&cfg, qkv_mlp_proj_kernel, maps, p, static_cast<uint16_t *>(q),
                             static_cast<uint16_t *>(k), static_cast<uint16_t *>(v),
