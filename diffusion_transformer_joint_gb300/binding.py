@@ -127,6 +127,18 @@ def _need_cuda(name, t, dtype):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _need_shape(name, t, shape):
+    """The C ABI takes pointers and sizes only: every tensor's shape is checked
+    here, before a kernel could read or write past it."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _need_ids(name, ids, n_axes):
+    if ids is not None and ids.numel() > 0 and (ids.dim() != 2 or int(ids.shape[1]) != n_axes):
+        raise ValueError(f"{name} must be [tokens, {n_axes}], got {tuple(ids.shape)}")
+
+
 def workspace_bytes(S: int, D: int = 128) -> int:
     """Smallest workspace of joint_rope_attention (status word + RoPE table)."""
     return int(load().flux_joint_rope_attention_workspace(int(S), int(D)))
@@ -168,6 +180,9 @@ def rope_tables(ids, axes_dims=AXES_DIMS, theta=THETA, cos_out=None, sin_out=Non
         cos_out = torch.empty((S, P), dtype=torch.float32, device=ids.device)
     if sin_out is None:
         sin_out = torch.empty((S, P), dtype=torch.float32, device=ids.device)
+    for name, t in (("cos_out", cos_out), ("sin_out", sin_out)):
+        _need_cuda(name, t, torch.float32)
+        _need_shape(name, t, (S, P))
     axes, n = _axes_array(axes_dims)
     if n != n_axes:
         raise ValueError("ids' last dimension must equal len(axes_dims)")
@@ -189,6 +204,8 @@ def rope_tables_packed(ids, axes_dims=AXES_DIMS, theta=THETA, out=None, stream=N
     P = sum(int(a) for a in axes_dims) // 2
     if out is None:
         out = torch.empty((S, P), dtype=torch.int32, device=ids.device)
+    _need_cuda("out", out, torch.int32)
+    _need_shape("out", out, (S, P))
     axes, n = _axes_array(axes_dims)
     if n != n_axes:
         raise ValueError("ids' last dimension must equal len(axes_dims)")
@@ -239,15 +256,23 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_cuda(name, t, torch.bfloat16)
     B, S, H, D = q.shape
+    _need_shape("k", k, q.shape)
+    _need_shape("v", v, q.shape)
     S_txt = 0 if txt_ids is None else int(txt_ids.shape[0])
     S_img = 0 if img_ids is None else int(img_ids.shape[0])
     for name, t in (("txt_ids", txt_ids), ("img_ids", img_ids)):
         if t is not None and t.numel() > 0:
             _need_cuda(name, t, torch.int32)
+            _need_ids(name, t, len(axes_dims))
+    if S_txt + S_img != S:
+        raise ValueError(f"the ids give {S_txt} + {S_img} tokens, q has {S}")
     if out is None:
         out = torch.empty_like(q)
     else:
         _need_cuda("out", out, torch.bfloat16)
+        _need_shape("out", out, q.shape)
+    if workspace is not None:
+        _need_cuda("workspace", workspace, torch.uint8)
     if workspace is None:
         n = workspace_shared_bytes(B, S, H, D) if share_k else 0
         if n == 0:
@@ -286,8 +311,16 @@ def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, k
     _need_cuda("table", table, torch.int32)
     _need_cuda("status", status, torch.int32)
     B, S, H, D = q.shape
+    _need_shape("k", k, q.shape)
+    _need_shape("v", v, q.shape)
+    _need_shape("table", table, (S, D // 2))
+    if status.numel() < 1:
+        raise ValueError("status must hold one int32")
     if out is None:
         out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        _need_shape("out", out, q.shape)
     if krot is None:
         krot = torch.empty(max(krot_bytes(B, S, H, D), 256), dtype=torch.uint8, device=q.device)
     if krot is False:
@@ -324,15 +357,26 @@ def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=AXES_DIMS, t
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need_cuda(name, t, torch.bfloat16)
     B, S, H, D = q.shape
+    _need_shape("k", k, q.shape)
+    _need_shape("v", v, q.shape)
     s_t, s_r, s_i = _rows(txt_ids), _rows(ref_ids), _rows(img_ids)
     for name, t in (("txt_ids", txt_ids), ("ref_ids", ref_ids), ("img_ids", img_ids)):
         if t is not None and t.numel() > 0:
             _need_cuda(name, t, torch.int32)
+            _need_ids(name, t, len(axes_dims))
+    if s_t + s_r + s_i != S:
+        raise ValueError(f"the ids give {s_t} + {s_r} + {s_i} tokens, q has {S}")
     out = torch.empty_like(q) if out is None else out
     if cache_k is None:
         cache_k = torch.empty((B, s_r, H, D), dtype=torch.bfloat16, device=q.device)
     if cache_v is None:
         cache_v = torch.empty((B, s_r, H, D), dtype=torch.bfloat16, device=q.device)
+    for name, t, shape in (("out", out, q.shape), ("cache_k", cache_k, (B, s_r, H, D)),
+                           ("cache_v", cache_v, (B, s_r, H, D))):
+        _need_cuda(name, t, torch.bfloat16)
+        _need_shape(name, t, shape)
+    if workspace is not None:
+        _need_cuda("workspace", workspace, torch.uint8)
     if workspace is None:
         n = extract_workspace_bytes(B, s_t, s_r, s_i, H, D)
         workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
@@ -355,11 +399,22 @@ def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES
     for name, t in (("q", q), ("k", k), ("v", v), ("cache_k", cache_k), ("cache_v", cache_v)):
         _need_cuda(name, t, torch.bfloat16)
     B, S, H, D = q.shape
+    _need_shape("k", k, q.shape)
+    _need_shape("v", v, q.shape)
     s_t, s_i, s_r = _rows(txt_ids), _rows(img_ids), int(cache_k.shape[1])
+    _need_shape("cache_k", cache_k, (B, s_r, H, D))
+    _need_shape("cache_v", cache_v, (B, s_r, H, D))
     for name, t in (("txt_ids", txt_ids), ("img_ids", img_ids)):
         if t is not None and t.numel() > 0:
             _need_cuda(name, t, torch.int32)
+            _need_ids(name, t, len(axes_dims))
+    if s_t + s_i != S:
+        raise ValueError(f"the ids give {s_t} + {s_i} tokens, q has {S}")
     out = torch.empty_like(q) if out is None else out
+    _need_cuda("out", out, torch.bfloat16)
+    _need_shape("out", out, q.shape)
+    if workspace is not None:
+        _need_cuda("workspace", workspace, torch.uint8)
     if workspace is None:
         n = cached_workspace_bytes(B, s_t, s_i, s_r, H, D)
         workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
@@ -402,6 +457,10 @@ def qkv_mlp_proj(x, w, H, mlp=None, q=None, k=None, v=None, act=None, status=Non
         status = torch.zeros(1, dtype=torch.int32, device=dev)
     for name, t in (("q", q), ("k", k), ("v", v), ("act", act)):
         _need_cuda(name, t, torch.bfloat16)
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_shape(name, t, lead + (H, 128))
+    _need_shape("act", act, lead + (mlp,))
+    _need_cuda("status", status, torch.int32)
     rc = lib.flux_qkv_mlp_proj(_ptr(x), _ptr(w), M, dim, int(H), 128, int(mlp), _ptr(q), _ptr(k),
                                _ptr(v), _ptr(act) if mlp > 0 else None, _ptr(status),
                                _stream_handle(stream))

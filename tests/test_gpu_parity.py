@@ -274,3 +274,34 @@ def test_more_items_than_blocks_all_outputs(B, H, S):
     txt, img = ids[:40], ids[40:]
     out = _run_gpu(q, k, v, txt, img)
     _compare(out, q, k, v, txt, img)
+
+
+def test_binding_rejects_mismatched_shapes():
+    """The C ABI takes pointers and sizes only; every binding checks tensor
+    shapes against the sizes it passes before anything is launched."""
+    B, S, H = 1, 80, 2
+    q = torch.zeros((B, S, H, 128), dtype=torch.bfloat16, device="cuda")
+    short = torch.zeros((B, S - 1, H, 128), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((S, 4), dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        binding.joint_rope_attention(q, short, q, ids[:16], ids[16:])
+    with pytest.raises(ValueError):
+        binding.joint_rope_attention(q, q, q, ids[:16], ids[17:])  # 79 ids for 80 tokens
+    with pytest.raises(ValueError):
+        binding.joint_rope_attention(q, q, q, ids[:16, :3], ids[16:])
+    with pytest.raises(ValueError):
+        binding.joint_rope_attention(q, q, q, ids[:16], ids[16:], out=short)
+    table = binding.rope_tables_packed(ids)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        binding.joint_rope_attention_tabled(q, q, q, table[:S - 1], status)
+    with pytest.raises(ValueError):
+        binding.attention_extract(q, q, q, ids[:16], ids[16:40], ids[41:])
+    with pytest.raises(ValueError):
+        binding.attention_cached(q, q, q, ids[:16], ids[16:], q[:, :8], q[:, :9])
+    x = torch.zeros((64, 128), dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros((3 * 256 + 2 * 128, 128), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        binding.qkv_mlp_proj(x, w, 2, 128, q=torch.zeros((63, 2, 128), dtype=torch.bfloat16,
+                                                           device="cuda"))
+    torch.cuda.synchronize()
