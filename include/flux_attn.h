@@ -21,6 +21,13 @@
  *     "核心引擎自注意力机制如何工作" (scaled dot-product attention:
  *     softmax(Q K^T / sqrt(d_k)) V with d_k the head size).
  *
+ * Entry points: the RoPE tables (fp32 and packed); the joint attention in one
+ * call (tables + attention) or with a caller-built table; both with the QK
+ * RMS normalisation fused in front of the rotation; the reference-image KV
+ * modes (extract, cached); and the single-stream block's fused input
+ * projection (Q, K, V and the SwiGLU-activated MLP input from one GEMM), the
+ * producer of the attention's inputs.
+ *
  * Conventions shared by every entry point:
  *   - Device pointers refer to memory on the CUDA device that is current on
  *     the calling thread; the caller owns every buffer, and the library
@@ -31,9 +38,10 @@
  *     argument returns a negative flux_status and enqueues nothing. A launch
  *     failure returns FLUX_ERR_CUDA.
  *   - Device-side failures (a bounded wait inside a kernel that ran out)
- *     never trap: the kernel records FLUX_ERR_DEVICE_TIMEOUT in the status
- *     word inside the caller's workspace and returns; read it with
- *     flux_query_status().
+ *     never trap: the kernel records FLUX_ERR_DEVICE_TIMEOUT in a status word
+ *     and returns. Entry points with a workspace keep the word at its start
+ *     (read it with flux_query_status()); the tabled attention and the
+ *     projection take a caller-owned device int32 instead.
  */
 #ifndef FLUX_ATTN_H
 #define FLUX_ATTN_H
@@ -55,7 +63,7 @@ typedef enum {
   FLUX_ERR_CUDA = -6,           /* a CUDA runtime call or launch failed */
   FLUX_ERR_DEVICE_TIMEOUT = -7, /* a kernel's bounded wait ran out (see flux_query_status) */
   FLUX_ERR_UNSUPPORTED = -8,    /* the current device is not sm_103 */
-  FLUX_ERR_ALIAS = -9           /* out overlaps q, k or v */
+  FLUX_ERR_ALIAS = -9           /* an output or scratch buffer overlaps an input or another output */
 } flux_status;
 
 /* Largest number of RoPE axes accepted (FLUX.2 uses 4). */
