@@ -49,7 +49,7 @@ const char *flux_status_string(int status) {
     case FLUX_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
     case FLUX_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device timeout)";
     case FLUX_ERR_UNSUPPORTED: return "the current device is not sm_103 (GB300)";
-    case FLUX_ERR_ALIAS: return "out or a scratch buffer overlaps q, k, v or out";
+    case FLUX_ERR_ALIAS: return "an output or scratch buffer overlaps an input or another output";
     default: return "unknown status";
   }
 }

@@ -23,7 +23,8 @@ with torch's float64 rms_norm and with its closed-form mean square, and the
 normalised attention with SDPA on inputs normalised and rotated separately.
 The reference KV modes agree with SDPA under an explicit boolean mask
 (extract) and over explicitly concatenated keys (cached), and a cache written
-in extract mode reproduces extract's text and image rows in cached mode.
+in extract mode reproduces extract's text and image rows in cached mode; with
+the QK norm they equal the plain modes on inputs normalised by torch.
 The fused single-stream projection places selected input channels exactly
 where the split puts them (Q, K, V heads, gate and linear halves), agrees with
 torch's float64 matmul and silu, and meets SiLU's closed forms.
@@ -114,6 +115,16 @@ class Oracle:
             P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
             ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P, ctypes.c_int64, P]
         lib.oracle_attention_cached.restype = ctypes.c_int
+        lib.oracle_qknorm_attention_extract.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int64, ctypes.c_int64, P, P, P, P, ctypes.c_double, P,
+            ctypes.c_int64, P, P, P]
+        lib.oracle_qknorm_attention_extract.restype = ctypes.c_int
+        lib.oracle_qknorm_attention_cached.argtypes = [
+            P, P, P, ctypes.c_int, ctypes.c_int64, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_int,
+            ctypes.c_double, ctypes.c_int64, P, P, ctypes.c_int64, P, P, P, P, ctypes.c_double, P,
+            ctypes.c_int64, P]
+        lib.oracle_qknorm_attention_cached.restype = ctypes.c_int
         lib.oracle_qkv_mlp_proj.argtypes = [
             P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64, P,
             ctypes.c_int64, P, P, P, P]
@@ -203,7 +214,7 @@ class Oracle:
 
 
     def attention_extract(self, q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                          theta=2000.0, rows=None):
+                          theta=2000.0, rows=None, qk_norm=None):
         """Extract mode over tokens [txt ; ref ; img]: (out [B, len(rows) or S, H, D],
         cache_k, cache_v [B, S_ref, H, D]) in fp64."""
         q = np.ascontiguousarray(q, dtype=np.float64)
@@ -220,16 +231,23 @@ class Oracle:
         out = np.empty((B, n_out, H, D))
         ck = np.empty((B, n_r, H, D))
         cv = np.empty((B, n_r, H, D))
-        rc = self.lib.oracle_attention_extract(
-            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size, float(theta),
-            n_t, n_r, None if rows_arr is None else _ptr(rows_arr), n_out, _ptr(out), _ptr(ck),
-            _ptr(cv))
+        if qk_norm is None:
+            rc = self.lib.oracle_attention_extract(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), n_t, n_r, None if rows_arr is None else _ptr(rows_arr), n_out,
+                _ptr(out), _ptr(ck), _ptr(cv))
+        else:
+            ws = [np.ascontiguousarray(w, dtype=np.float64) for w in qk_norm[:4]]
+            rc = self.lib.oracle_qknorm_attention_extract(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), n_t, n_r, *[_ptr(w) for w in ws], float(qk_norm[4]),
+                None if rows_arr is None else _ptr(rows_arr), n_out, _ptr(out), _ptr(ck), _ptr(cv))
         if rc != 0:
             raise ValueError("oracle_attention_extract: bad arguments")
         return out, ck, cv
 
     def attention_cached(self, q, k, v, txt_ids, img_ids, cache_k, cache_v,
-                         axes_dims=(32, 32, 32, 32), theta=2000.0, rows=None):
+                         axes_dims=(32, 32, 32, 32), theta=2000.0, rows=None, qk_norm=None):
         """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; fp64 out."""
         q = np.ascontiguousarray(q, dtype=np.float64)
         k = np.ascontiguousarray(k, dtype=np.float64)
@@ -244,10 +262,17 @@ class Oracle:
         rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
         n_out = S if rows_arr is None else rows_arr.size
         out = np.empty((B, n_out, H, D))
-        rc = self.lib.oracle_attention_cached(
-            _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size, float(theta),
-            n_t, _ptr(ck), _ptr(cv), ck.shape[1], None if rows_arr is None else _ptr(rows_arr),
-            n_out, _ptr(out))
+        if qk_norm is None:
+            rc = self.lib.oracle_attention_cached(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), n_t, _ptr(ck), _ptr(cv), ck.shape[1],
+                None if rows_arr is None else _ptr(rows_arr), n_out, _ptr(out))
+        else:
+            ws = [np.ascontiguousarray(w, dtype=np.float64) for w in qk_norm[:4]]
+            rc = self.lib.oracle_qknorm_attention_cached(
+                _ptr(q), _ptr(k), _ptr(v), B, S, H, D, _ptr(ids), _ptr(axes), axes.size,
+                float(theta), n_t, _ptr(ck), _ptr(cv), ck.shape[1], *[_ptr(w) for w in ws],
+                float(qk_norm[4]), None if rows_arr is None else _ptr(rows_arr), n_out, _ptr(out))
         if rc != 0:
             raise ValueError("oracle_attention_cached: bad arguments")
         return out
@@ -298,14 +323,15 @@ def rms_norm(x, w, eps=1e-6):
 
 
 def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=(32, 32, 32, 32),
-                      theta=2000.0, rows=None):
-    return default().attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims, theta, rows)
+                      theta=2000.0, rows=None, qk_norm=None):
+    return default().attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims, theta, rows,
+                                       qk_norm)
 
 
 def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=(32, 32, 32, 32),
-                     theta=2000.0, rows=None):
+                     theta=2000.0, rows=None, qk_norm=None):
     return default().attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims,
-                                      theta, rows)
+                                      theta, rows, qk_norm)
 
 
 def qkv_mlp_proj(x, w, H, D=128, mlp=None, rows=None):

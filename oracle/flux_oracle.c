@@ -49,7 +49,9 @@
  *      keys only while text and image queries attend to every token, and the
  *      reference K / V are stored to the cache; in "cached" mode the sequence
  *      is [txt, img] and the cached reference K / V are inserted between the
- *      text and the image keys and values).
+ *      text and the image keys and values). With the QK normalisation of
+ *      step 4 the modes see q and k normalised first (reference tokens take
+ *      the image stream's weights), so the cache holds normalised, rotated K.
  *
  *   6. The single-stream block's fused input projection ("Diffusers 中
  *      Flux2Transformer2DModel 全面解析", section "内部架构双流块与单流块": one
@@ -486,4 +488,64 @@ int oracle_qkv_mlp_proj(const double *x, const double *w, int64_t M, int dim, in
     }
   }
   return 0;
+}
+
+/* Steps 4 and 5 together: the KV modes with the QK RMS normalisation before
+ * RoPE. q and k are normalised token by token (the first S_txt tokens, text,
+ * with the text weights; every other token, reference or image, with the
+ * image weights) and then go through the mode unchanged; the cache holds the
+ * normalised, rotated K. */
+static int qk_normed_copies(const double *q, const double *k, int B, int64_t S, int H, int D,
+                            const double *qw_txt, const double *kw_txt, const double *qw_img,
+                            const double *kw_img, int64_t S_txt, double eps, double **qn,
+                            double **kn) {
+  if (qw_txt == NULL || kw_txt == NULL || qw_img == NULL || kw_img == NULL || S_txt < 0 ||
+      S_txt > S || !(eps >= 0.0))
+    return -1;
+  const size_t n = (size_t)B * (size_t)S * (size_t)H * (size_t)D;
+  *qn = (double *)malloc(sizeof(double) * (n ? n : 1));
+  *kn = (double *)malloc(sizeof(double) * (n ? n : 1));
+  for (int b = 0; b < B; ++b)
+    for (int64_t t = 0; t < S; ++t)
+      for (int h = 0; h < H; ++h) {
+        const int64_t off = (((int64_t)b * S + t) * H + h) * D;
+        oracle_rms_norm_vec(q + off, t < S_txt ? qw_txt : qw_img, D, eps, *qn + off);
+        oracle_rms_norm_vec(k + off, t < S_txt ? kw_txt : kw_img, D, eps, *kn + off);
+      }
+  return 0;
+}
+
+int oracle_qknorm_attention_extract(const double *q, const double *k, const double *v, int B,
+                                    int64_t S, int H, int D, const int32_t *ids,
+                                    const int32_t *axes_dims, int n_axes, double theta,
+                                    int64_t S_txt, int64_t S_ref, const double *qw_txt,
+                                    const double *kw_txt, const double *qw_img,
+                                    const double *kw_img, double eps, const int64_t *rows,
+                                    int64_t n_rows, double *out, double *cache_k,
+                                    double *cache_v) {
+  double *qn = NULL, *kn = NULL;
+  if (qk_normed_copies(q, k, B, S, H, D, qw_txt, kw_txt, qw_img, kw_img, S_txt, eps, &qn, &kn))
+    return -1;
+  const int rc = oracle_attention_extract(qn, kn, v, B, S, H, D, ids, axes_dims, n_axes, theta,
+                                          S_txt, S_ref, rows, n_rows, out, cache_k, cache_v);
+  free(qn);
+  free(kn);
+  return rc;
+}
+
+int oracle_qknorm_attention_cached(const double *q, const double *k, const double *v, int B,
+                                   int64_t S, int H, int D, const int32_t *ids,
+                                   const int32_t *axes_dims, int n_axes, double theta,
+                                   int64_t S_txt, const double *cache_k, const double *cache_v,
+                                   int64_t S_ref, const double *qw_txt, const double *kw_txt,
+                                   const double *qw_img, const double *kw_img, double eps,
+                                   const int64_t *rows, int64_t n_rows, double *out) {
+  double *qn = NULL, *kn = NULL;
+  if (qk_normed_copies(q, k, B, S, H, D, qw_txt, kw_txt, qw_img, kw_img, S_txt, eps, &qn, &kn))
+    return -1;
+  const int rc = oracle_attention_cached(qn, kn, v, B, S, H, D, ids, axes_dims, n_axes, theta,
+                                         S_txt, cache_k, cache_v, S_ref, rows, n_rows, out);
+  free(qn);
+  free(kn);
+  return rc;
 }

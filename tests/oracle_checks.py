@@ -405,6 +405,42 @@ def check_extract_then_cached_reproduces_rows(orc):
     assert np.array_equal(sub2, out2[:, [2, 0]])
 
 
+def check_kv_modes_with_qk_norm(orc):
+    """Extract and cached with the QK norm equal the plain modes on q and k
+    normalised beforehand by torch's float64 rms_norm (text tokens with the
+    text weights, reference and image tokens with the image weights)."""
+    rng = _rng(43)
+    B, H, D = 1, 2, 16
+    S_t, S_r, S_i = 5, 9, 7
+    S = S_t + S_r + S_i
+    ids = _rand_ids(rng, S)
+    txt, ref, img = ids[:S_t], ids[S_t:S_t + S_r], ids[S_t + S_r:]
+    q, k, v = (rng.standard_normal((B, S, H, D)) for _ in range(3))
+    ws = [rng.uniform(0.3, 1.7, D) for _ in range(4)]  # q txt, k txt, q img, k img
+    eps = 1e-6
+
+    def normed(x, w_txt, w_img, n_txt):
+        y = np.empty_like(x)
+        y[:, :n_txt] = _torch_rms_norm(x[:, :n_txt], w_txt, eps)
+        y[:, n_txt:] = _torch_rms_norm(x[:, n_txt:], w_img, eps)
+        return y
+
+    axes = (4, 4, 4, 4)
+    qn, kn = normed(q, ws[0], ws[2], S_t), normed(k, ws[1], ws[3], S_t)
+    ref_out, ref_ck, ref_cv = orc.attention_extract(qn, kn, v, txt, ref, img, axes, 50.0)
+    out, ck, cv = orc.attention_extract(q, k, v, txt, ref, img, axes, 50.0,
+                                        qk_norm=tuple(ws) + (eps,))
+    assert np.allclose(out, ref_out, rtol=1e-12, atol=1e-13)
+    assert np.allclose(ck, ref_ck, rtol=1e-12, atol=1e-13) and np.array_equal(cv, ref_cv)
+    keep = np.r_[0:S_t, S_t + S_r:S]
+    q2, k2, v2 = q[:, keep], k[:, keep], v[:, keep]
+    q2n, k2n = normed(q2, ws[0], ws[2], S_t), normed(k2, ws[1], ws[3], S_t)
+    ref2 = orc.attention_cached(q2n, k2n, v2, txt, img, ck, cv, axes, 50.0)
+    got2 = orc.attention_cached(q2, k2, v2, txt, img, ck, cv, axes, 50.0,
+                                qk_norm=tuple(ws) + (eps,))
+    assert np.allclose(got2, ref2, rtol=1e-12, atol=1e-13)
+
+
 def _torch_silu(x):
     import torch
 
@@ -501,6 +537,7 @@ ALL_CHECKS = [
     check_extract_mode_vs_masked_sdpa,
     check_cached_mode_vs_concatenated_sdpa,
     check_extract_then_cached_reproduces_rows,
+    check_kv_modes_with_qk_norm,
     check_proj_selection_weights,
     check_proj_vs_torch_matmul,
     check_proj_silu_closed_forms,

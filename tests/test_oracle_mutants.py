@@ -78,6 +78,10 @@ MUTANTS = {
     # off-by-one in the key loop
     "skip_last_key": ("for (int64_t j = 0; j < S; ++j) {\n      double acc",
                       "for (int64_t j = 0; j < S - 1; ++j) {\n      double acc"),
+    "kvnorm_k_with_q_weights": ("oracle_rms_norm_vec(k + off, t < S_txt ? kw_txt : kw_img, D, eps, *kn + off);",
+                                "oracle_rms_norm_vec(k + off, t < S_txt ? qw_txt : qw_img, D, eps, *kn + off);"),
+    "kvnorm_refs_as_text": ("oracle_rms_norm_vec(q + off, t < S_txt ? qw_txt : qw_img, D, eps, *qn + off);",
+                            "oracle_rms_norm_vec(q + off, t < S_txt + 4 ? qw_txt : qw_img, D, eps, *qn + off);"),
     "proj_gate_linear_swapped": ("proj_dot(xi, w, dim, n_out, 3 * inner + j);",
                                  "proj_dot(xi, w, dim, n_out, 3 * inner + mlp + j);"),
     "proj_no_sigmoid": ("act[r * mlp + j] = g / (1.0 + exp(-g)) * u;",
