@@ -463,15 +463,19 @@ def run_kv(args, rank, world, local_rank):
             else binding.cached_workspace_bytes(w.B, S_t, S_i, S_r, w.H, w.D))
     ws = torch.zeros(int(n_ws), dtype=torch.uint8, device=dev)
     stream = torch.cuda.Stream(device=dev)
+    qk_norm = None
+    if args.qk_norm:  # synthetic learned weights in [0.5, 1.5), one vector per stream and tensor
+        g = torch.Generator().manual_seed(7)
+        qk_norm = tuple((0.5 + torch.rand(w.D, generator=g)).to(dev) for _ in range(4)) + (1e-6,)
 
     def call(ts, outs, st):
         if mode == "extract":
             binding.attention_extract(*ts, *ids, out=outs[0], cache_k=outs[1], cache_v=outs[2],
-                                      workspace=ws, stream=st)
+                                      workspace=ws, stream=st, qk_norm=qk_norm)
         else:
             q, k, v, ck, cv = ts
             binding.attention_cached(q, k, v, ids[0], ids[1], ck, cv, out=outs[0], workspace=ws,
-                                     stream=st)
+                                     stream=st, qk_norm=qk_norm)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -517,11 +521,12 @@ def run_kv(args, rank, world, local_rank):
             d_in, d_ids, d_out = ln["in"], ln["ids"], ln["out"]
             if mode == "extract":
                 binding.attention_extract(*d_in, *d_ids, out=d_out[0], cache_k=d_out[1],
-                                          cache_v=d_out[2], workspace=ln["ws"], stream=st)
+                                          cache_v=d_out[2], workspace=ln["ws"], stream=st,
+                                          qk_norm=qk_norm)
             else:
                 q, k, v, ck, cv = d_in
                 binding.attention_cached(q, k, v, d_ids[0], d_ids[1], ck, cv, out=d_out[0],
-                                         workspace=ln["ws"], stream=st)
+                                         workspace=ln["ws"], stream=st, qk_norm=qk_norm)
             for h, d in zip(ln["hout"], d_out):
                 h.copy_(d, non_blocking=True)
 
@@ -559,6 +564,8 @@ def run_kv(args, rank, world, local_rank):
             "step": ("two table kernels, the attention kernel over 3 segments, two cache copies"
                      if mode == "extract" else
                      "one table kernel, the attention kernel (cache read in place, not rotated)"),
+            "qk_norm": ("fused QK RMS norm before RoPE (eps 1e-6, synthetic per-stream weights)"
+                        if args.qk_norm else "none"),
         },
         "roofline": {
             "bound": "tensor", "kernel": "whole call (tables + attention + copies)",

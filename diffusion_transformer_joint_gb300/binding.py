@@ -28,6 +28,7 @@ EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_atten
            "flux_joint_qknorm_rope_attention", "flux_joint_qknorm_rope_attention_tabled",
            "flux_joint_rope_attention_extract_workspace", "flux_joint_rope_attention_extract",
            "flux_joint_rope_attention_cached_workspace", "flux_joint_rope_attention_cached",
+           "flux_joint_qknorm_rope_attention_extract", "flux_joint_qknorm_rope_attention_cached",
            "flux_qkv_mlp_proj", "flux_query_status", "flux_status_string")
 
 
@@ -91,6 +92,14 @@ def load(path: str | None = None):
             lib.flux_joint_rope_attention_cached.argtypes = [
                 V, V, V, V, I64, V, I64, V, V, I64, I32, I32, I32, V, I32, D, V, V, SZ, V]
             lib.flux_joint_rope_attention_cached.restype = I32
+            lib.flux_joint_qknorm_rope_attention_extract.argtypes = [
+                V, V, V, V, I64, V, I64, V, I64, I32, I32, I32, V, I32, D, V, V, V, V, F, V, V, V, V,
+                SZ, V]
+            lib.flux_joint_qknorm_rope_attention_extract.restype = I32
+            lib.flux_joint_qknorm_rope_attention_cached.argtypes = [
+                V, V, V, V, I64, V, I64, V, V, I64, I32, I32, I32, V, I32, D, V, V, V, V, F, V, V,
+                SZ, V]
+            lib.flux_joint_qknorm_rope_attention_cached.restype = I32
             lib.flux_qkv_mlp_proj.argtypes = [V, V, I64, I32, I32, I32, I64, V, V, V, V, V, V]
             lib.flux_qkv_mlp_proj.restype = I32
             lib.flux_query_status.argtypes = [V, V]
@@ -349,8 +358,11 @@ def _rows(ids):
 
 
 def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA,
-                      out=None, cache_k=None, cache_v=None, workspace=None, stream=None):
-    """Extract mode over tokens [txt ; ref ; img]: returns (out, cache_k, cache_v)."""
+                      out=None, cache_k=None, cache_v=None, workspace=None, stream=None,
+                      qk_norm=None):
+    """Extract mode over tokens [txt ; ref ; img]: returns (out, cache_k, cache_v).
+    ``qk_norm`` as for joint_rope_attention (reference tokens take the image
+    weights; the cache then holds the normalised, rotated K)."""
     import torch
 
     lib = load()
@@ -381,18 +393,29 @@ def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=AXES_DIMS, t
         n = extract_workspace_bytes(B, s_t, s_r, s_i, H, D)
         workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
     axes, na = _axes_array(axes_dims)
-    rc = lib.flux_joint_rope_attention_extract(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(ref_ids), s_r, _ptr(img_ids), s_i, B,
-        H, D, axes, na, float(theta), _ptr(out), _ptr(cache_k), _ptr(cache_v), _ptr(workspace),
-        workspace.numel(), _stream_handle(stream))
+    if qk_norm is None:
+        name = "flux_joint_rope_attention_extract"
+        rc = lib.flux_joint_rope_attention_extract(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(ref_ids), s_r, _ptr(img_ids), s_i,
+            B, H, D, axes, na, float(theta), _ptr(out), _ptr(cache_k), _ptr(cache_v),
+            _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    else:
+        name = "flux_joint_qknorm_rope_attention_extract"
+        ws, eps = _norm_args(qk_norm, q.device)
+        rc = lib.flux_joint_qknorm_rope_attention_extract(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(ref_ids), s_r, _ptr(img_ids), s_i,
+            B, H, D, axes, na, float(theta), *[_ptr(w) for w in ws], eps, _ptr(out),
+            _ptr(cache_k), _ptr(cache_v), _ptr(workspace), workspace.numel(),
+            _stream_handle(stream))
     if rc != 0:
-        raise FluxError("flux_joint_rope_attention_extract", rc, lib)
+        raise FluxError(name, rc, lib)
     return out, cache_k, cache_v
 
 
 def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES_DIMS,
-                     theta=THETA, out=None, workspace=None, stream=None):
-    """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; returns out."""
+                     theta=THETA, out=None, workspace=None, stream=None, qk_norm=None):
+    """Cached mode: queries [txt ; img] over keys [txt ; cache ; img]; returns out.
+    ``qk_norm`` normalises q and the keys of k (the cache is used as stored)."""
     import torch
 
     lib = load()
@@ -419,12 +442,21 @@ def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES
         n = cached_workspace_bytes(B, s_t, s_i, s_r, H, D)
         workspace = torch.empty(max(int(n), 256), dtype=torch.uint8, device=q.device)
     axes, na = _axes_array(axes_dims)
-    rc = lib.flux_joint_rope_attention_cached(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(img_ids), s_i, _ptr(cache_k),
-        _ptr(cache_v), s_r, B, H, D, axes, na, float(theta), _ptr(out), _ptr(workspace),
-        workspace.numel(), _stream_handle(stream))
+    if qk_norm is None:
+        name = "flux_joint_rope_attention_cached"
+        rc = lib.flux_joint_rope_attention_cached(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(img_ids), s_i, _ptr(cache_k),
+            _ptr(cache_v), s_r, B, H, D, axes, na, float(theta), _ptr(out), _ptr(workspace),
+            workspace.numel(), _stream_handle(stream))
+    else:
+        name = "flux_joint_qknorm_rope_attention_cached"
+        ws, eps = _norm_args(qk_norm, q.device)
+        rc = lib.flux_joint_qknorm_rope_attention_cached(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(img_ids), s_i, _ptr(cache_k),
+            _ptr(cache_v), s_r, B, H, D, axes, na, float(theta), *[_ptr(w) for w in ws], eps,
+            _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
     if rc != 0:
-        raise FluxError("flux_joint_rope_attention_cached", rc, lib)
+        raise FluxError(name, rc, lib)
     return out
 
 

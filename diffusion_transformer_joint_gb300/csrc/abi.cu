@@ -293,13 +293,12 @@ size_t flux_joint_rope_attention_extract_workspace(int B, int64_t S_txt, int64_t
          flux::exchange_bytes(B, S, S, H, sg, n);
 }
 
-int flux_joint_rope_attention_extract(const void *q, const void *k, const void *v,
-                                      const int32_t *txt_ids, int64_t S_txt,
-                                      const int32_t *ref_ids, int64_t S_ref,
-                                      const int32_t *img_ids, int64_t S_img, int B, int H, int D,
-                                      const int32_t *axes_dims, int n_axes, double theta,
-                                      void *out, void *cache_k, void *cache_v, void *workspace,
-                                      size_t workspace_bytes, void *stream) {
+static int extract_call(const void *q, const void *k, const void *v, const int32_t *txt_ids,
+                        int64_t S_txt, const int32_t *ref_ids, int64_t S_ref,
+                        const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                        const int32_t *axes_dims, int n_axes, double theta,
+                        const float *const norm_w[4], float eps, void *out, void *cache_k,
+                        void *cache_v, void *workspace, size_t workspace_bytes, void *stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
     return FLUX_ERR_NULL;
   if ((S_txt > 0 && txt_ids == nullptr) || (S_ref > 0 && ref_ids == nullptr) ||
@@ -308,6 +307,10 @@ int flux_joint_rope_attention_extract(const void *q, const void *k, const void *
   if (S_txt < 0 || S_ref < 0 || S_img < 0) return FLUX_ERR_SHAPE;
   const int64_t S = S_txt + S_ref + S_img;
   if (!kv_shape_ok(B, H, D, S)) return FLUX_ERR_SHAPE;
+  if (norm_w != nullptr) {
+    const int nc = check_norm(norm_w, eps, S_txt, S);
+    if (nc != FLUX_OK) return nc;
+  }
   flux::RopePairs pp;
   const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
   if (rc != FLUX_OK) return rc;
@@ -351,8 +354,12 @@ int flux_joint_rope_attention_extract(const void *q, const void *k, const void *
     return FLUX_ERR_CUDA;
   flux::AttnSegment sg[flux::kMaxSegments];
   const int n = extract_segments(S_txt, S_ref, S_img, sg);
+  // with the norm, reference tokens (after the text) take the image weights
+  flux::QkNormArgs nargs{};
+  if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, sg, n,
-                                      nullptr, xbuf, nullptr, st) != cudaSuccess)
+                                      nullptr, xbuf, norm_w != nullptr ? &nargs : nullptr,
+                                      st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   if (S_ref > 0) {
     // the cache: every key tile was rotated once into the exchange buffer's
@@ -385,13 +392,12 @@ size_t flux_joint_rope_attention_cached_workspace(int B, int64_t S_txt, int64_t 
          flux::exchange_bytes(B, S_q, S_q, H, &all, 1);
 }
 
-int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v,
-                                     const int32_t *txt_ids, int64_t S_txt,
-                                     const int32_t *img_ids, int64_t S_img, const void *cache_k,
-                                     const void *cache_v, int64_t S_ref, int B, int H, int D,
-                                     const int32_t *axes_dims, int n_axes, double theta,
-                                     void *out, void *workspace, size_t workspace_bytes,
-                                     void *stream) {
+static int cached_call(const void *q, const void *k, const void *v, const int32_t *txt_ids,
+                       int64_t S_txt, const int32_t *img_ids, int64_t S_img,
+                       const void *cache_k, const void *cache_v, int64_t S_ref, int B, int H,
+                       int D, const int32_t *axes_dims, int n_axes, double theta,
+                       const float *const norm_w[4], float eps, void *out, void *workspace,
+                       size_t workspace_bytes, void *stream) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
     return FLUX_ERR_NULL;
   if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr) ||
@@ -400,6 +406,10 @@ int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v
   if (S_txt < 0 || S_img < 0 || S_ref < 0 || S_txt + S_img < 1) return FLUX_ERR_SHAPE;
   const int64_t S_q = S_txt + S_img, S_k = S_q + S_ref;
   if (!kv_shape_ok(B, H, D, S_k)) return FLUX_ERR_SHAPE;
+  if (norm_w != nullptr) {
+    const int nc = check_norm(norm_w, eps, S_txt, S_q);
+    if (nc != FLUX_OK) return nc;
+  }
   flux::RopePairs pp;
   const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
   if (rc != FLUX_OK) return rc;
@@ -438,10 +448,63 @@ int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v
     return FLUX_ERR_CUDA;
   const flux::AttnSegment all{0, S_q, 0, S_q, 0, S_ref};
   const flux::PreRotatedKV cache{cache_k, cache_v, S_ref};
+  // the norm acts on q and the keys of k; the cached keys arrive normalised
+  flux::QkNormArgs nargs{};
+  if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S_q, S_q, H, &all, 1,
-                                      &cache, xbuf, nullptr, st) != cudaSuccess)
+                                      &cache, xbuf, norm_w != nullptr ? &nargs : nullptr,
+                                      st) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
+}
+
+int flux_joint_rope_attention_extract(const void *q, const void *k, const void *v,
+                                      const int32_t *txt_ids, int64_t S_txt,
+                                      const int32_t *ref_ids, int64_t S_ref,
+                                      const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                      const int32_t *axes_dims, int n_axes, double theta,
+                                      void *out, void *cache_k, void *cache_v, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+  return extract_call(q, k, v, txt_ids, S_txt, ref_ids, S_ref, img_ids, S_img, B, H, D,
+                      axes_dims, n_axes, theta, nullptr, 0.f, out, cache_k, cache_v, workspace,
+                      workspace_bytes, stream);
+}
+
+int flux_joint_qknorm_rope_attention_extract(
+    const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
+    const int32_t *ref_ids, int64_t S_ref, const int32_t *img_ids, int64_t S_img, int B, int H,
+    int D, const int32_t *axes_dims, int n_axes, double theta, const float *q_norm_txt,
+    const float *k_norm_txt, const float *q_norm_img, const float *k_norm_img, float eps,
+    void *out, void *cache_k, void *cache_v, void *workspace, size_t workspace_bytes,
+    void *stream) {
+  const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
+  return extract_call(q, k, v, txt_ids, S_txt, ref_ids, S_ref, img_ids, S_img, B, H, D,
+                      axes_dims, n_axes, theta, w, eps, out, cache_k, cache_v, workspace,
+                      workspace_bytes, stream);
+}
+
+int flux_joint_rope_attention_cached(const void *q, const void *k, const void *v,
+                                     const int32_t *txt_ids, int64_t S_txt,
+                                     const int32_t *img_ids, int64_t S_img, const void *cache_k,
+                                     const void *cache_v, int64_t S_ref, int B, int H, int D,
+                                     const int32_t *axes_dims, int n_axes, double theta,
+                                     void *out, void *workspace, size_t workspace_bytes,
+                                     void *stream) {
+  return cached_call(q, k, v, txt_ids, S_txt, img_ids, S_img, cache_k, cache_v, S_ref, B, H, D,
+                     axes_dims, n_axes, theta, nullptr, 0.f, out, workspace, workspace_bytes,
+                     stream);
+}
+
+int flux_joint_qknorm_rope_attention_cached(
+    const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
+    const int32_t *img_ids, int64_t S_img, const void *cache_k, const void *cache_v,
+    int64_t S_ref, int B, int H, int D, const int32_t *axes_dims, int n_axes, double theta,
+    const float *q_norm_txt, const float *k_norm_txt, const float *q_norm_img,
+    const float *k_norm_img, float eps, void *out, void *workspace, size_t workspace_bytes,
+    void *stream) {
+  const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
+  return cached_call(q, k, v, txt_ids, S_txt, img_ids, S_img, cache_k, cache_v, S_ref, B, H, D,
+                     axes_dims, n_axes, theta, w, eps, out, workspace, workspace_bytes, stream);
 }
 
 int flux_query_status(const void *workspace, void *stream) {

@@ -321,6 +321,32 @@ int flux_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim, int H, i
                       int64_t mlp_hidden, void *q, void *k, void *v, void *act, int32_t *status,
                       void *stream);
 
+/*
+ * flux_joint_qknorm_rope_attention_extract / _cached: the two KV modes with
+ * the QK RMS normalisation before RoPE (as flux_joint_qknorm_rope_attention:
+ * text tokens, the first S_txt, with the text weights; every other token,
+ * reference or image, with the image weights). In extract mode the cache
+ * receives the normalised, rotated K; in cached mode the cached K is used as
+ * stored (normalised and rotated already) while q and the keys of k are
+ * normalised. Workspace sizes as for the plain modes; other arguments and
+ * return codes as flux_joint_rope_attention_extract / _cached and
+ * flux_joint_qknorm_rope_attention.
+ */
+int flux_joint_qknorm_rope_attention_extract(
+    const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
+    const int32_t *ref_ids, int64_t S_ref, const int32_t *img_ids, int64_t S_img, int B, int H,
+    int D, const int32_t *axes_dims, int n_axes, double theta, const float *q_norm_txt,
+    const float *k_norm_txt, const float *q_norm_img, const float *k_norm_img, float eps,
+    void *out, void *cache_k, void *cache_v, void *workspace, size_t workspace_bytes,
+    void *stream);
+int flux_joint_qknorm_rope_attention_cached(
+    const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
+    const int32_t *img_ids, int64_t S_img, const void *cache_k, const void *cache_v,
+    int64_t S_ref, int B, int H, int D, const int32_t *axes_dims, int n_axes, double theta,
+    const float *q_norm_txt, const float *k_norm_txt, const float *q_norm_img,
+    const float *k_norm_img, float eps, void *out, void *workspace, size_t workspace_bytes,
+    void *stream);
+
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
  * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
  * on every device that loads this library, held until the process exits. */

@@ -155,3 +155,50 @@ def test_two_reference_edit_workload_sampled_rows():
     r2 = oracle.attention_cached(qk.float().numpy(), kk.float().numpy(), vk.float().numpy(), txt,
                                  img, ck.float().cpu().numpy(), cv.float().cpu().numpy(), rows=rows2)
     _bar(out2.float().cpu().numpy()[:, rows2], r2)
+
+
+def _norm_weights(seed, eps=1e-6):
+    rng = np.random.default_rng(seed)
+    return [rng.uniform(0.5, 1.5, 128).astype(np.float32) for _ in range(4)], eps
+
+
+def _normed(x, w_txt, w_img, n_txt, eps):
+    """x / sqrt(mean x^2 + eps) * w per head vector, in float64 (for error bounds)."""
+    x = x.astype(np.float64)
+    r = 1.0 / np.sqrt((x * x).mean(axis=-1, keepdims=True) + eps)
+    w = np.concatenate([np.broadcast_to(w_txt, (n_txt, 128)),
+                        np.broadcast_to(w_img, (x.shape[1] - n_txt, 128))])[None, :, None, :]
+    return x * r * w
+
+
+@pytest.mark.parametrize("B,H,S_t,S_r,S_i", [(1, 2, 16, 64, 64), (1, 1, 33, 200, 290)])
+def test_kv_modes_with_qk_norm(B, H, S_t, S_r, S_i):
+    """Extract then cached with the QK RMS normalisation before RoPE: outputs
+    against the oracle, the cache's K against the normalised, rotated keys,
+    and cached mode fed with the GPU's own cache."""
+    S = S_t + S_r + S_i
+    q, k, v = _inputs(B, S, H, 1200 + S)
+    ids = W.random_ids(S, 1204 + S, 0, 300)
+    txt, ref, img = ids[:S_t], ids[S_t:S_t + S_r], ids[S_t + S_r:]
+    ws, eps = _norm_weights(1205 + S)
+    norm_dev = tuple(_dev(w) for w in ws) + (eps,)
+    norm_np = tuple(ws) + (eps,)
+    out, ck, cv = binding.attention_extract(_dev(q), _dev(k), _dev(v), _dev(txt), _dev(ref),
+                                            _dev(img), qk_norm=norm_dev)
+    torch.cuda.synchronize()
+    r_out, r_ck, _ = oracle.attention_extract(q.float().numpy(), k.float().numpy(),
+                                              v.float().numpy(), txt, ref, img, qk_norm=norm_np)
+    _bar(out.float().cpu().numpy(), r_out)
+    kn = _normed(k.float().numpy(), ws[1], ws[3], S_t, eps)[:, S_t:S_t + S_r]
+    _check_cache_k(ck.float().cpu().numpy(), r_ck, kn)
+    assert torch.equal(cv.cpu(), v[:, S_t:S_t + S_r])
+    keep = np.r_[0:S_t, S_t + S_r:S]
+    qk, kk, vk = q[:, keep].contiguous(), k[:, keep].contiguous(), v[:, keep].contiguous()
+    out2 = binding.attention_cached(_dev(qk), _dev(kk), _dev(vk), _dev(txt), _dev(img), ck, cv,
+                                    qk_norm=norm_dev)
+    torch.cuda.synchronize()
+    ref2 = oracle.attention_cached(qk.float().numpy(), kk.float().numpy(), vk.float().numpy(), txt,
+                                   img, ck.float().cpu().numpy(), cv.float().cpu().numpy(),
+                                   qk_norm=norm_np)
+    _bar(out2.float().cpu().numpy(), ref2)
+    _bar(out2.float().cpu().numpy(), out[:, keep].float().cpu().numpy().astype(np.float64))
