@@ -214,3 +214,25 @@ def test_qkv_mlp_proj_argument_checks(lib):
     assert call(k=128 * MB + 4096) == -9   # k overlaps q
     assert call(act=1024) == -9            # act overlaps x
     assert call(v=64 * MB + 64) == -9      # v overlaps w
+
+
+def test_kv_modes_with_norm_argument_checks(lib):
+    P = ctypes.c_void_p
+    axes = (ctypes.c_int32 * 4)(32, 32, 32, 32)
+    need = lib.flux_joint_rope_attention_extract_workspace(1, 16, 32, 32, 2, 128)
+    w = [P(200 * 1024 * 1024 + 512 * i) for i in range(4)]
+
+    def extract(weights=w, eps=1e-6):
+        return lib.flux_joint_qknorm_rope_attention_extract(
+            P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(3072), 32, P(2048), 32, 1, 2, 128,
+            axes, 4, 2000.0, *weights, eps, P(48 * 1024 * 1024), P(96 * 1024 * 1024),
+            P(100 * 1024 * 1024), P(256 * 65536), need, None)
+
+    assert extract(weights=[w[0], None, w[2], w[3]]) == -1       # every weight vector needed
+    assert extract(weights=[P(200 * 1024 * 1024 + 4)] + w[1:]) == -4  # 16-byte aligned
+    assert extract(eps=-1.0) == -2                                 # eps >= 0
+    cneed = lib.flux_joint_rope_attention_cached_workspace(1, 16, 32, 8, 2, 128)
+    assert lib.flux_joint_qknorm_rope_attention_cached(
+        P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(2048), 32, P(300 * 1024),
+        P(200 * 1024), 8, 1, 2, 128, axes, 4, 2000.0, None, w[1], w[2], w[3], 1e-6,
+        P(48 * 1024 * 1024), P(256 * 65536), cneed, None) == -1
