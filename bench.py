@@ -297,6 +297,7 @@ def run_ours(args, rank, world, local_rank):
             "algorithmic_flops_per_launch": flops_step,
             "algorithmic_bytes_per_launch": w.io_bytes,
             "avg_launch_ms": round(attn_avg_ms, 4),
+            "launch_ms_p10_p50_p90": [round(x, 4) for x in _percentiles(attn_ms, (10, 50, 90))],
         },
         "clocks": clocks.summary(),
         "e2e": {"value": round(whole_job_tflops(flops_step, world, 1, e2e["ms_per_step"]), 2),
@@ -793,6 +794,41 @@ def cpu_baseline(w, target_s=12.0):
                       f"{w.name} against all {w.S} keys, fp64, {t:.1f} s"}
 
 
+def _percentiles(xs, ps):
+    xs = sorted(xs)
+    return [xs[min(len(xs) - 1, max(0, int(round(p / 100.0 * (len(xs) - 1)))))] for p in ps]
+
+
+def cpu_report(seconds=3.0):
+    """The oracle on every workload: a bounded sample of query rows timed with
+    all host threads and with one (one head's rows for the one-thread run),
+    as fp64 GFLOP/s. Printed as its own JSON line; no GPU is used."""
+    import numpy as np
+
+    import oracle
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    oracle.build()
+    threads = oracle.default_threads()
+    report = []
+    for w in W.WORKLOADS.values():
+        inputs = _oracle_inputs(w)
+        rows = _rows_for(w, seconds, threads, inputs)
+        t = _oracle_sample(w, rows, threads, *inputs)
+        many = 4 * w.B * w.H * rows.size * w.S * w.D / t / 1e9
+        q, k, v, txt, img = inputs  # one head, one thread
+        one_head = [x[:, :, :1] for x in (q, k, v)]
+        rows1 = np.linspace(0, w.S - 1, min(64, w.S)).astype(np.int64)
+        t1 = _oracle_sample(w, rows1, 1, *one_head, txt, img)
+        single = 4 * w.B * rows1.size * w.S * w.D / t1 / 1e9
+        report.append({"workload": w.name, "S": w.S, "H": w.H,
+                       "gflops_all_threads": round(many, 2), "threads": threads,
+                       "rows_sampled": int(rows.size), "seconds": round(t, 2),
+                       "gflops_one_thread": round(single, 3),
+                       "one_thread_sample": f"{rows1.size} rows x 1 head"})
+    return {"cpu_report": report, "kind": "oracle", "dtype": "f64"}
+
+
 def run_reference(args, rank, world):
     """The oracle on the host cores: each step is a bounded sample of the same
     workload; the line carries the same metric and unit as ours."""
@@ -843,6 +879,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--kv-mode", choices=("extract", "cached"), default=None,
                     help="time a reference-image KV-mode call on an edit workload instead")
+    ap.add_argument("--cpu-report", action="store_true",
+                    help="time the fp64 oracle on every workload (all threads and one); no GPU")
     ap.add_argument("--proj", action="store_true",
                     help="time the fused single-stream QKV+MLP input projection instead")
     ap.add_argument("--qk-norm", action="store_true",
@@ -854,7 +892,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    if args.impl == "reference":
+    if args.cpu_report:
+        line = cpu_report() if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         if world > 1:
