@@ -305,3 +305,18 @@ def test_binding_rejects_mismatched_shapes():
         binding.qkv_mlp_proj(x, w, 2, 128, q=torch.zeros((63, 2, 128), dtype=torch.bfloat16,
                                                            device="cuda"))
     torch.cuda.synchronize()
+
+
+def test_long_multi_batch_sequence_sampled_rows():
+    """B = 2, S = 32845 (a ragged last tile), H = 3: 774 work items, row
+    offsets past 2^24 elements per tensor and two batch elements sharing one
+    id set. Sampled rows of both batch elements against the oracle."""
+    B, H, S = 2, 3, 32768 + 77
+    q = W.normal_bf16((B, S, H, 128), 1401)
+    k = W.normal_bf16((B, S, H, 128), 1402)
+    v = W.normal_bf16((B, S, H, 128), 1403)
+    ids = W.random_ids(S, 1404, 0, 900)
+    txt, img = ids[:512], ids[512:]
+    out = _run_gpu(q, k, v, txt, img)
+    rows = _sample_rows(S, 512, 10, seed=1405)
+    _compare(out, q, k, v, txt, img, rows=rows)
