@@ -98,11 +98,6 @@ struct ProjMaps {
   CUtensorMap x, w, q, k, v, act;
 };
 
-__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-  const bool ok = mbar_wait(bar, parity, abort_flag);
-  return __all_sync(0xffffffffu, ok);
-}
-
 __device__ __forceinline__ void drain(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity) && clock64() - t0 < kWaitBudgetCycles) {

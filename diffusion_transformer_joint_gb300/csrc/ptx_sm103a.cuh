@@ -385,16 +385,11 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) 
 
 // ------------------------------------------- cross-CTA hand-off in global
 
-// Strong relaxed load / store at GPU scope (flag words shared between CTAs).
-__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t *p) {
-  uint64_t v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
 // Two adjacent flag words (16-byte aligned), each read with relaxed strength.
 __device__ __forceinline__ void ld_relaxed_gpu_v2_u64(const uint64_t *p, uint64_t &a, uint64_t &b) {
   asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
+// A flag word stored with relaxed strength at GPU scope.
 __device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -413,15 +408,6 @@ __device__ __forceinline__ void st_global_v4(void *p, uint4 v) {
                "r"(v.w)
                : "memory");
 }
-__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 // ------------------------------------------------------- TMEM loads/stores
 
 // Each thread of the warp reads 32 consecutive 32-bit columns of its lane.
@@ -564,14 +550,6 @@ __device__ __forceinline__ uint4 ld_global_nc_v4(const void *p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
-__device__ __forceinline__ float4 ld_global_nc_f4(const float *p) {
-  float4 v;
-  asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
                : "l"(p));
   return v;
 }
