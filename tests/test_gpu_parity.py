@@ -320,3 +320,38 @@ def test_long_multi_batch_sequence_sampled_rows():
     out = _run_gpu(q, k, v, txt, img)
     rows = _sample_rows(S, 512, 10, seed=1405)
     _compare(out, q, k, v, txt, img, rows=rows)
+
+
+def _close(a, b, max_abs=2 * MAX_ABS, mean_abs=2 * MEAN_ABS):
+    """Two kernel outputs, each within the bar of the exact result, agree
+    within twice the bar."""
+    err = (a.float() - b.float()).abs()
+    assert float(err.max()) <= max_abs and float(err.mean()) <= mean_abs
+
+
+def test_gpu_id_translation_invariance():
+    """Adding a constant to every token's id on an axis leaves the output
+    unchanged (RoPE logits depend on id differences only): the kernel's output
+    for shifted ids equals its output for the original ids, to rounding."""
+    B, H, S = 1, 3, 333
+    q, k, v = (W.normal_bf16((B, S, H, 128), 1500 + i).cuda() for i in range(3))
+    ids = W.random_ids(S, 1503, 0, 200)
+    shift = np.array([7, -40, 123, 5], dtype=np.int32)
+    a = binding.joint_rope_attention(q, k, v, _dev(ids[:50]), _dev(ids[50:]))
+    b = binding.joint_rope_attention(q, k, v, _dev(ids[:50] + shift), _dev(ids[50:] + shift))
+    torch.cuda.synchronize()
+    _close(a, b)
+
+
+def test_gpu_token_permutation_equivariance():
+    """Permuting the tokens together with their ids permutes the output rows
+    (non-causal attention); the key order only changes summation order."""
+    B, H, S = 2, 2, 300
+    q, k, v = (W.normal_bf16((B, S, H, 128), 1510 + i) for i in range(3))
+    ids = W.random_ids(S, 1513, 0, 200)
+    perm = np.random.default_rng(1514).permutation(S)
+    a = _run_gpu(q, k, v, ids[:64], ids[64:])
+    qp, kp, vp = (x[:, perm].contiguous() for x in (q, k, v))
+    idp = ids[perm]
+    b = _run_gpu(qp, kp, vp, idp[:64], idp[64:])
+    _close(a[:, torch.from_numpy(perm).cuda()], b)
