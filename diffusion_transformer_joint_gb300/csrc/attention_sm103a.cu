@@ -170,11 +170,23 @@ struct QkNorm {
   float eps;
 };
 
-// Per-channel scale of this thread's 8 channels (16-byte chunk c16) of a row
-// whose 8 bf16 values are `x`: the 16 lanes holding one row sum their squares
-// across shuffles, so all 32 lanes of the warp must call this together.
+// This thread's 8 norm weights of each stream (16-byte chunk c16), loaded once
+// per rotation call rather than once per row: a thread keeps the same chunk of
+// every row it rotates. Only the kNorm paths call this (both pointers set).
+struct NormW {
+  float4 t0, t1, i0, i1;
+};
+__device__ __forceinline__ NormW load_norm_w(const QkNorm &nm, int c16) {
+  const float4 *t = reinterpret_cast<const float4 *>(nm.w_txt + c16 * 8);
+  const float4 *i = reinterpret_cast<const float4 *>(nm.w_img + c16 * 8);
+  return NormW{__ldg(t), __ldg(t + 1), __ldg(i), __ldg(i + 1)};
+}
+
+// Per-channel scale of this thread's 8 channels (weights `nw`) of a row whose
+// 8 bf16 values are `x`: the 16 lanes holding one row sum their squares across
+// shuffles, so all 32 lanes of the warp must call this together.
 __device__ __forceinline__ void qk_norm_scales(const uint4 &x, const QkNorm &nm, int64_t token,
-                                               int c16, float (&sc)[8]) {
+                                               const NormW &nw, float (&sc)[8]) {
   const uint32_t wv[4] = {x.x, x.y, x.z, x.w};
   float ss = 0.f;
 #pragma unroll
@@ -186,8 +198,8 @@ __device__ __forceinline__ void qk_norm_scales(const uint4 &x, const QkNorm &nm,
 #pragma unroll
   for (int o = 1; o < 16; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float r = rsqrtf(ss * (1.0f / kD) + nm.eps);
-  const float4 *w = reinterpret_cast<const float4 *>((token < nm.s_txt ? nm.w_txt : nm.w_img) + c16 * 8);
-  const float4 w0 = __ldg(w), w1 = __ldg(w + 1);
+  const bool txt = token < nm.s_txt;
+  const float4 w0 = txt ? nw.t0 : nw.i0, w1 = txt ? nw.t1 : nw.i1;
   sc[0] = r * w0.x; sc[1] = r * w0.y; sc[2] = r * w0.z; sc[3] = r * w0.w;
   sc[4] = r * w1.x; sc[5] = r * w1.y; sc[6] = r * w1.z; sc[7] = r * w1.w;
 }
@@ -196,11 +208,11 @@ __device__ __forceinline__ void qk_norm_scales(const uint4 &x, const QkNorm &nm,
 // them first when kNorm.
 template <bool kNorm>
 __device__ __forceinline__ uint4 rope_chunk(const uint4 &x, const uint4 &cs, const QkNorm &nm,
-                                            int64_t token, int c16) {
+                                            int64_t token, const NormW &nw) {
   uint4 o;
   if (kNorm) {
     float sc[8];
-    qk_norm_scales(x, nm, token, c16, sc);
+    qk_norm_scales(x, nm, token, nw, sc);
     o.x = rope_pair_scaled(x.x, cs.x, sc[0], sc[1]);
     o.y = rope_pair_scaled(x.y, cs.y, sc[2], sc[3]);
     o.z = rope_pair_scaled(x.z, cs.z, sc[4], sc[5]);
@@ -239,6 +251,7 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
                                             uint16_t *grow, int64_t row_stride) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
+  const NormW nw = kNorm ? load_norm_w(nm, c16) : NormW{};
   // batches of rows (four, or two with the norm's extra registers): all
   // loads of a batch in flight together
   constexpr int kBatch = kNorm ? 2 : 4;
@@ -254,7 +267,7 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int r = half * 64 + (i0 + i) * 8 + rsub;
-      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, c16);
+      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, nw);
       st_shared_v4(tile + sw128_offset(r, c16), o);
       if (kPublish && r < rows_valid) st_global_v4(grow + r * row_stride + c16 * 8, o);
     }
@@ -275,6 +288,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
                                                    int64_t tok0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
+  const NormW nw = kNorm ? load_norm_w(nm, c16) : NormW{};
 #pragma unroll 1
   for (int i0 = 0; (kNorm ? 8 * i0 : rsub + 8 * i0) < nrows; i0 += 2) {
     uint4 w[2], cs[2];
@@ -291,7 +305,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const int r = rsub + 8 * (i0 + i);
-      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, c16);
+      const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, nw);
       if (r < nrows) st_global_v4(dst + r * row_stride + c16 * 8, o);
     }
   }
