@@ -34,6 +34,44 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def _declared_signatures():
+    """name -> (return type, [parameter types]) from the header, as C type strings."""
+    sigs = {}
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for ret, name, params in re.findall(
+                r"([A-Za-z_][A-Za-z0-9_ ]*?\**)\s*\b(flux_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+            types = []
+            for prm in params.split(","):
+                prm = prm.strip()
+                types.append("ptr" if "*" in prm else prm.rsplit(None, 1)[0].replace("const ", ""))
+            sigs[name] = ("ptr" if "*" in ret else ret.split()[-1], types)
+    return sigs
+
+
+_CTYPE_OF = {"ptr": (ctypes.c_void_p, ctypes.c_char_p), "int": (ctypes.c_int,),
+             "int64_t": (ctypes.c_int64,), "size_t": (ctypes.c_size_t,),
+             "double": (ctypes.c_double,), "float": (ctypes.c_float,)}
+
+
+def test_binding_marshals_every_argument_as_declared(lib):
+    # a wrong ctypes width (an int where the header has int64_t, a float for a
+    # double) would pass garbage through the ABI without any error
+    sigs = _declared_signatures()
+    assert set(binding.EXPORTS) <= set(sigs)
+    for name in binding.EXPORTS:
+        ret, params = sigs[name]
+        fn = getattr(lib, name)
+        assert len(fn.argtypes) == len(params), name
+        for i, (have, want) in enumerate(zip(fn.argtypes, params)):
+            assert have in _CTYPE_OF[want], (name, i, have, want)
+        assert fn.restype in _CTYPE_OF[ret], (name, fn.restype, ret)
+
+
 def test_status_strings(lib):
     for code in binding.STATUS:
         assert lib.flux_status_string(code)
