@@ -234,17 +234,21 @@ def unpack_table(packed):
     return halves[..., 0].float(), halves[..., 1].float()
 
 
-def _norm_args(qk_norm, device):
-    """(q_txt, k_txt, q_img, k_img, eps) -> four fp32 CUDA [128] tensors and eps."""
+def _norm_args(qk_norm, device, D=128):
+    """(q_txt, k_txt, q_img, k_img, eps) -> four fp32 CUDA [D] tensors and eps
+    (the kernels read D weights from each pointer)."""
     import torch
 
+    if len(qk_norm) != 5:
+        raise ValueError("qk_norm must be (q_norm_txt, k_norm_txt, q_norm_img, k_norm_img, eps)")
     *ws, eps = qk_norm
-    ts = []
-    for name, w in zip(("q_norm_txt", "k_norm_txt", "q_norm_img", "k_norm_img"), ws):
-        if not isinstance(w, torch.Tensor):
-            w = torch.as_tensor(w, dtype=torch.float32, device=device)
+    names = ("q_norm_txt", "k_norm_txt", "q_norm_img", "k_norm_img")
+    ts = [w if isinstance(w, torch.Tensor) else torch.as_tensor(w, dtype=torch.float32,
+                                                                device=device) for w in ws]
+    for name, w in zip(names, ts):
+        _need_shape(name, w, (D,))
+    for name, w in zip(names, ts):
         _need_cuda(name, w, torch.float32)
-        ts.append(w)
     return ts, float(eps)
 
 
@@ -294,7 +298,7 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
             n, float(theta), _ptr(out), _ptr(workspace), workspace.numel(), _stream_handle(stream))
         name = "flux_joint_rope_attention"
     else:
-        ws, eps = _norm_args(qk_norm, q.device)
+        ws, eps = _norm_args(qk_norm, q.device, D)
         rc = lib.flux_joint_qknorm_rope_attention(
             _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, D, axes,
             n, float(theta), *[_ptr(w) for w in ws], eps, _ptr(out), _ptr(workspace),
@@ -343,7 +347,7 @@ def joint_rope_attention_tabled(q, k, v, table, status, out=None, stream=None, k
                                                   _stream_handle(stream))
         name = "flux_joint_rope_attention_tabled"
     else:
-        ws, eps = _norm_args(qk_norm, q.device)
+        ws, eps = _norm_args(qk_norm, q.device, D)
         rc = lib.flux_joint_qknorm_rope_attention_tabled(
             _ptr(q), _ptr(k), _ptr(v), _ptr(table), B, S, H, D, int(s_txt),
             *[_ptr(w) for w in ws], eps, _ptr(out), _ptr(status), kp, kn, _stream_handle(stream))
@@ -401,7 +405,7 @@ def attention_extract(q, k, v, txt_ids, ref_ids, img_ids, axes_dims=AXES_DIMS, t
             _ptr(workspace), workspace.numel(), _stream_handle(stream))
     else:
         name = "flux_joint_qknorm_rope_attention_extract"
-        ws, eps = _norm_args(qk_norm, q.device)
+        ws, eps = _norm_args(qk_norm, q.device, D)
         rc = lib.flux_joint_qknorm_rope_attention_extract(
             _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(ref_ids), s_r, _ptr(img_ids), s_i,
             B, H, D, axes, na, float(theta), *[_ptr(w) for w in ws], eps, _ptr(out),
@@ -450,7 +454,7 @@ def attention_cached(q, k, v, txt_ids, img_ids, cache_k, cache_v, axes_dims=AXES
             workspace.numel(), _stream_handle(stream))
     else:
         name = "flux_joint_qknorm_rope_attention_cached"
-        ws, eps = _norm_args(qk_norm, q.device)
+        ws, eps = _norm_args(qk_norm, q.device, D)
         rc = lib.flux_joint_qknorm_rope_attention_cached(
             _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), s_t, _ptr(img_ids), s_i, _ptr(cache_k),
             _ptr(cache_v), s_r, B, H, D, axes, na, float(theta), *[_ptr(w) for w in ws], eps,
@@ -477,6 +481,8 @@ def qkv_mlp_proj(x, w, H, mlp=None, q=None, k=None, v=None, act=None, status=Non
     inner = H * 128
     if mlp is None:
         mlp = (int(w.shape[0]) - 3 * inner) // 2
+    if mlp < 0:
+        raise ValueError(f"w has {int(w.shape[0])} rows, fewer than the {3 * inner} of q, k, v")
     if tuple(w.shape) != (3 * inner + 2 * mlp, dim):
         raise ValueError(f"w must be [{3 * inner + 2 * mlp}, {dim}], got {tuple(w.shape)}")
     dev = x.device

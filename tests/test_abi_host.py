@@ -274,3 +274,20 @@ def test_kv_modes_with_norm_argument_checks(lib):
         P(16), P(64 * 1024), P(128 * 1024), P(1024), 16, P(2048), 32, P(300 * 1024),
         P(200 * 1024), 8, 1, 2, 128, axes, 4, 2000.0, None, w[1], w[2], w[3], 1e-6,
         P(48 * 1024 * 1024), P(256 * 65536), cneed, None) == -1
+
+
+def test_norm_weight_shapes_checked_in_the_binding():
+    # the kernels read 128 fp32 weights through each pointer: a shorter vector
+    # is refused before anything reaches the library
+    import torch
+
+    good = torch.ones(128)
+    with pytest.raises(ValueError, match="shape"):
+        binding._norm_args((torch.ones(64), good, good, good, 1e-6), "cpu")
+    with pytest.raises(ValueError, match="shape"):
+        binding._norm_args((good, good, good, torch.ones(2, 128), 1e-6), "cpu")
+    with pytest.raises(ValueError, match="qk_norm must be"):
+        binding._norm_args((good, good, good, 1e-6), "cpu")
+    # right shapes pass that check and stop at the device check (no CPU path)
+    with pytest.raises(ValueError, match="CUDA"):
+        binding._norm_args((good, good, good, good, 1e-6), "cpu")
