@@ -10,7 +10,6 @@ trap, no fault: afterwards the context is still usable and the regular
 library computes the correct result on the same stream.
 """
 import ctypes
-import os
 import shutil
 import subprocess
 import time

@@ -4,7 +4,6 @@ Each mutant is the oracle's own C source with one textual change, compiled
 into a temporary library on the CPU. A mutant that passes every pin would
 mean the pins cannot tell that mistake from the method.
 """
-import os
 
 import pytest
 

@@ -10,7 +10,6 @@ not depend on any earlier test, so it passes alone in a fresh process too.
 """
 import ctypes
 
-import numpy as np
 import pytest
 
 from diffusion_transformer_joint_gb300 import binding, build
