@@ -52,3 +52,22 @@ def test_profiled_traffic_is_none_or_positive():
     # a summary taken on another source reads as unknown
     assert bench._profiled_traffic(bench.PROJ_PROFILE_SUMMARY, bench.KERNEL_SOURCE,
                                    "dram_bytes_per_launch_klein9b") is None
+
+
+def test_committed_profiles_are_of_the_current_kernel_sources():
+    # the bench's traffic figures come from the ncu summaries in profiles/; each
+    # summary records the hash of the source it was taken on, so a kernel edit
+    # without a new capture shows up here instead of as a silent null
+    w = W.WORKLOADS["klein9b"]
+    attn = bench._profiled_traffic()
+    assert attn is not None
+    # DRAM traffic cannot be below the algorithmic bytes; far above them would
+    # mean re-reads (the exchange buffer accounts for the measured extra)
+    assert w.io_bytes <= attn <= 1.5 * w.io_bytes
+    proj = bench._profiled_traffic(bench.PROJ_PROFILE_SUMMARY, bench.PROJ_SOURCE,
+                                   "dram_bytes_per_launch_klein9b")
+    M, dim, mlp = W.proj_dims(w)
+    n_out = 3 * w.H * 128 + 2 * mlp
+    proj_io = 2 * (M * dim + n_out * dim + M * (3 * w.H * 128 + mlp))
+    assert proj is not None
+    assert proj_io <= proj <= 1.5 * proj_io
