@@ -1250,14 +1250,9 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     maps.qrot = maps.q;
   }
   // persistent: one CTA per SM, work items handed out round robin
-  static int sm_count[64];
-  if (sm_count[dev] == 0) {
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    sm_count[dev] = n;
-  }
-  const unsigned grid = static_cast<unsigned>(items < sm_count[dev] ? items : sm_count[dev]);
+  const int sms = sm_count_current_device();
+  if (sms == 0) return cudaErrorUnknown;
+  const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   const uint16_t *qg = static_cast<const uint16_t *>(q), *kg = static_cast<const uint16_t *>(k);
   uint16_t *og = static_cast<uint16_t *>(out);
   if (norm != nullptr) {

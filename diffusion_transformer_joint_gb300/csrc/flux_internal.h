@@ -10,6 +10,10 @@
 
 namespace flux {
 
+// Number of SMs of the current device (cached per device ordinal, atomically);
+// 0 if the runtime cannot tell.
+int sm_count_current_device();
+
 // Largest rotation-pair count of one head (head width 512).
 constexpr int kMaxPairs = 256;
 

@@ -17,6 +17,7 @@
 //
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "flux_internal.h"
@@ -59,6 +60,18 @@ __global__ void __launch_bounds__(256) rope_tables_kernel(const int32_t *__restr
 
 }  // namespace
 
+int sm_count_current_device() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  int n = cached[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
 int make_rope_pairs(const int32_t *axes_dims, int n_axes, double theta, RopePairs *pp) {
   if (axes_dims == nullptr) return FLUX_ERR_NULL;
   if (n_axes < 1 || n_axes > FLUX_MAX_AXES || !(theta > 0.0) || !std::isfinite(theta))
@@ -90,7 +103,9 @@ cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *i
   const int64_t S = S0 + S1;
   const dim3 block(64, 4);
   int64_t blocks = (S + block.y - 1) / block.y;
-  if (blocks > 8 * 152) blocks = 8 * 152;
+  const int sms = sm_count_current_device();
+  if (sms == 0) return cudaErrorUnknown;
+  if (blocks > 8 * sms) blocks = 8 * sms;
   if (blocks < 1) blocks = 1;
   if (fmt == TableFormat::kF32Pair)
     rope_tables_kernel<TableFormat::kF32Pair><<<static_cast<unsigned>(blocks), block, 0, stream>>>(
