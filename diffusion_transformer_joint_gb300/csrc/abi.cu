@@ -16,6 +16,10 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return a0 < b0 + nb && b0 < a0 + na;
 }
 
+}  // namespace
+
+namespace flux {
+
 // sm_103 check, cached per device ordinal.
 int check_device() {
   static std::atomic<int> cached[64];  // 0 unknown, 1 ok, -1 unsupported
@@ -34,7 +38,9 @@ int check_device() {
   return c == 1 ? FLUX_OK : FLUX_ERR_UNSUPPORTED;
 }
 
-}  // namespace
+}  // namespace flux
+
+using flux::check_device;
 
 extern "C" {
 

@@ -10,6 +10,10 @@
 
 namespace flux {
 
+// FLUX_OK if the current device is an sm_103 part (cached per device),
+// FLUX_ERR_UNSUPPORTED if not, FLUX_ERR_CUDA if the runtime cannot tell.
+int check_device();
+
 // Number of SMs of the current device (cached per device ordinal, atomically);
 // 0 if the runtime cannot tell.
 int sm_count_current_device();

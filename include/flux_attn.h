@@ -348,8 +348,9 @@ int flux_joint_qknorm_rope_attention_cached(
     void *stream);
 
 /* Largest joint sequence (S_txt + S_img) that flux_joint_rope_attention_noalloc
- * accepts. Its scratch array is 256 + 2 * 32768 * 64 * 4 bytes (16 MiB + 256 B)
- * on every device that loads this library, held until the process exits. */
+ * accepts. Its scratch array is 256 + 32768 * 64 * 4 bytes (8 MiB + 256 B: the
+ * status word and one packed (cos, sin) table) on every device that loads this
+ * library, held until the process exits. */
 #define FLUX_NOALLOC_MAX_TOKENS 32768
 
 /*
@@ -361,30 +362,43 @@ int flux_joint_qknorm_rope_attention_cached(
  * streams. The caller still passes inputs and outputs; nothing is allocated
  * or freed (no cudaMalloc, no cudaFree, no allocating library routine).
  *
- * Scratch (RoPE tables and the status word) lives in one fixed file-scope
+ * Scratch (the status word and the RoPE table) lives in one fixed file-scope
  * device array of the library, one per device. Consequences:
  *   - S_txt + S_img above FLUX_NOALLOC_MAX_TOKENS returns FLUX_ERR_SHAPE and
  *     launches nothing; D must be 128 as for the regular entry point.
+ *   - The array has no room for the rotated-K exchange buffer, so every
+ *     thread block rotates every K tile it loads. The output is bit-identical
+ *     to flux_joint_rope_attention's on the same inputs.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins on the device.
  *   - Every call shares the one array and it keeps the last call's contents.
- *     Each call clears the status word and rewrites the tables before the
+ *     Each call clears the status word and rewrites the table before the
  *     attention kernel reads them, so results do not depend on earlier
  *     calls; but calls that overlap on the GPU (different streams, or
  *     different host threads, without ordering between them) race on the
  *     array and give undefined results. Order them on one stream.
- *   - The device status word is not readable through this entry point; a
- *     device timeout is not reported (use the regular entry point with
- *     flux_query_status when that matters).
  * Arguments, layouts and the other return codes are those of
- * flux_joint_rope_attention; FLUX_ERR_CUDA also when the address lookup fails.
+ * flux_joint_rope_attention, with the device check made first; FLUX_ERR_CUDA
+ * also when the address lookup fails.
  */
 int flux_joint_rope_attention_noalloc(const void *q, const void *k, const void *v,
                                       const int32_t *txt_ids, int64_t S_txt,
                                       const int32_t *img_ids, int64_t S_img, int B, int H, int D,
                                       const int32_t *axes_dims, int n_axes, double theta,
                                       void *out, void *stream);
+
+/*
+ * flux_joint_rope_attention_noalloc_status: synchronises `stream` and returns
+ * the device status word that the last flux_joint_rope_attention_noalloc call
+ * on the current device left in the library's array: FLUX_OK, or
+ * FLUX_ERR_DEVICE_TIMEOUT when its kernel gave up a bounded wait (its output
+ * is then not valid). Pass the stream that call was made on; a later call
+ * clears the word. FLUX_ERR_CUDA when the synchronisation, the copy or the
+ * address lookup fails; FLUX_ERR_UNSUPPORTED on a device that is not sm_103.
+ * Allocates nothing.
+ */
+int flux_joint_rope_attention_noalloc_status(void *stream);
 
 /*
  * flux_query_status: synchronises `stream`, reads the device status word of
