@@ -15,6 +15,7 @@ import torch
 import oracle
 from diffusion_transformer_joint_gb300 import binding, build
 from diffusion_transformer_joint_gb300 import workloads as W
+from tests.oracle_parallel import by_head as _by_head
 
 pytestmark = pytest.mark.gpu
 
@@ -124,10 +125,11 @@ def test_extract_then_cached_on_the_gpu():
     _bar(out2.float().cpu().numpy(), out[:, keep].float().cpu().numpy().astype(np.float64))
 
 
-def test_two_reference_edit_workload_sampled_rows():
+def test_two_reference_edit_workload_all_outputs():
     """The klein-9B two-reference edit shape as the KV pipeline runs it: one
     extract call over [txt 512 ; ref 8192 ; img 4096], then a cached call
-    over [txt ; img] with that cache. Sampled rows against the oracle."""
+    over [txt ; img] with that cache. Every output of both calls against the
+    oracle; the whole cache against the oracle's."""
     w = W.WORKLOADS["klein9b_edit2"]
     S_t, S_i, S_r = w.S_txt, 4096, w.S_img - 4096
     q0, k0, v0 = W.workload_qkv(w)  # [txt ; img ; refs]: reorder to [txt ; refs ; img]
@@ -139,22 +141,18 @@ def test_two_reference_edit_workload_sampled_rows():
     out, ck, cv = binding.attention_extract(_dev(q), _dev(k), _dev(v), _dev(txt), _dev(ref),
                                             _dev(img))
     torch.cuda.synchronize()
-    rng = np.random.default_rng(11)
-    rows = np.unique(np.concatenate([[0, S_t - 1, S_t, S_t + S_r - 1, S_t + S_r, w.S - 1],
-                                     rng.integers(0, w.S, 14)]))
-    r_out, r_ck, _ = oracle.attention_extract(q.float().numpy(), k.float().numpy(),
-                                              v.float().numpy(), txt, ref, img, rows=rows)
-    _bar(out.float().cpu().numpy()[:, rows], r_out)
-    _check_cache_k(ck.float().cpu().numpy(), r_ck, k[:, S_t:S_t + S_r].float().numpy())
+    qn, kn, vn = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    r_out, r_ck, _ = _by_head(oracle.attention_extract, w.H, qn, kn, vn, txt, ref, img)
+    _bar(out.float().cpu().numpy(), r_out)
+    _check_cache_k(ck.float().cpu().numpy(), r_ck, kn[:, S_t:S_t + S_r])
     assert torch.equal(cv.cpu(), v[:, S_t:S_t + S_r])
     keep = np.r_[0:S_t, S_t + S_r:w.S]
     qk, kk, vk = q[:, keep].contiguous(), k[:, keep].contiguous(), v[:, keep].contiguous()
     out2 = binding.attention_cached(_dev(qk), _dev(kk), _dev(vk), _dev(txt), _dev(img), ck, cv)
     torch.cuda.synchronize()
-    rows2 = np.unique(np.concatenate([[0, S_t - 1, S_t, S_t + S_i - 1], rng.integers(0, S_t + S_i, 12)]))
-    r2 = oracle.attention_cached(qk.float().numpy(), kk.float().numpy(), vk.float().numpy(), txt,
-                                 img, ck.float().cpu().numpy(), cv.float().cpu().numpy(), rows=rows2)
-    _bar(out2.float().cpu().numpy()[:, rows2], r2)
+    r2 = _by_head(oracle.attention_cached, w.H, qk.float().numpy(), kk.float().numpy(),
+                  vk.float().numpy(), txt, img, ck.float().cpu().numpy(), cv.float().cpu().numpy())
+    _bar(out2.float().cpu().numpy(), r2)
 
 
 def _norm_weights(seed, eps=1e-6):

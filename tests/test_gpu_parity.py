@@ -1,10 +1,12 @@
 """GPU parity: the CUDA path through the C-ABI against the fp64 oracle.
 
 Tolerance (bf16 inputs, fp32 accumulation): max |gpu - oracle| <= 1e-2 and
-mean |gpu - oracle| <= 1e-3 over the compared outputs. Small cases compare
-every output element; the full-size workloads compare sampled query rows
-(all batch elements and heads of each row), chosen to cover the first and
-last tokens, the 128-row tile edges, the text/image boundary and random rows.
+mean |gpu - oracle| <= 1e-3 over every output element of the tiny, klein-4B,
+klein-9B, dev-32B and two-reference edit workloads and of the small and ragged
+shapes. Only the long multi-batch sequence (S 32845, not one of the five
+workloads) compares sampled query rows (all batch elements and heads of each
+row). Large-logit cases are compared with the exact oracle under the bound of
+a first-order rounding-error model (tests/error_model.py).
 """
 import numpy as np
 import pytest
@@ -12,6 +14,7 @@ import torch
 
 import oracle
 from diffusion_transformer_joint_gb300 import binding, build
+from tests import error_model as EM
 from diffusion_transformer_joint_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -207,6 +210,51 @@ def test_peaked_softmax_online_rescale():
     _compare(out, qr, kr, v, zero[:33], zero[33:], max_abs=bound)
 
 
+def _exact_rotated(x, c, s, norm=None):
+    """The oracle's exact rows before and after the rotation (optionally RMS
+    normalised first with (w_txt, w_img, S_txt, eps))."""
+    xd = x.double().numpy()
+    if norm is not None:
+        w_txt, w_img, s_txt, eps = norm
+        xd = np.concatenate([oracle.rms_norm(xd[:, :s_txt], w_txt, eps),
+                             oracle.rms_norm(xd[:, s_txt:], w_img, eps)], axis=1)
+    return xd, oracle.rope_apply(xd, c, s)
+
+
+def test_peaked_softmax_against_exact_oracle():
+    """q scaled by 8 (logit standard deviation 8: few keys carry each row)
+    against the plain oracle of the inputs. The bf16 storage of the rotated q
+    and k moves each logit by about 2e-3 of its scale, here ~0.02, which the
+    bar for N(0, 1) inputs (1e-2 / 1e-3) does not allow for. The bound is the
+    first-order rounding-error model's, computed from the exact quantities
+    before the kernel's output is looked at: per element Z(N) sigma plus the
+    fixed term, and the mean within RMS(sigma). The fp16 table alone (rest
+    in fp64) stays inside the plain bar."""
+    B, H, S = 1, 2, 517
+    q = W.normal_bf16((B, S, H, 128), 45, scale=8.0)
+    k = W.normal_bf16((B, S, H, 128), 46)
+    v = W.normal_bf16((B, S, H, 128), 47)
+    ids = W.random_ids(S, 48, 0, 600)
+    c, s = oracle.rope_tables(ids)
+    qx, qh = _exact_rotated(q, c, s)
+    kx, kh = _exact_rotated(k, c, s)
+    exact = oracle.joint_rope_attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                                        ids[:33], ids[33:])
+    sigma = EM.predicted_sigma(qh, kh, v.double().numpy(), exact,
+                               EM.rotated_error_var(qx, c, s, qh),
+                               EM.rotated_error_var(kx, c, s, kh))
+    out = _run_gpu(q, k, v, ids[:33], ids[33:])
+    EM.check(out.float().cpu().numpy(), exact, sigma, float(v.abs().max()))
+    # the fp16 table's own cost against the plain oracle
+    c16 = c.astype(np.float16).astype(np.float64)
+    s16 = s.astype(np.float16).astype(np.float64)
+    zero = np.zeros_like(ids)
+    t16 = oracle.joint_rope_attention(oracle.rope_apply(qx, c16, s16),
+                                      oracle.rope_apply(kx, c16, s16), v.double().numpy(),
+                                      zero[:33], zero[33:])
+    assert np.abs(t16 - exact).max() <= MAX_ABS and np.abs(t16 - exact).mean() <= MEAN_ABS
+
+
 def test_identical_keys_give_mean_of_v():
     B, H, S = 1, 2, 300
     ids = np.tile(np.array([[3, 1, 4, 1]], np.int32), (S, 1))
@@ -247,19 +295,20 @@ def test_deterministic_and_stream_ordered():
 
 
 @pytest.mark.parametrize("name", ["klein4b", "klein9b", "dev32b", "klein9b_edit2"])
-def test_full_workload_sampled_rows(name):
+def test_full_workload_all_outputs(name):
+    """Every output element of the workload against the oracle (fp64, all host
+    threads), then the same bits from the smallest workspace (no rotated-K
+    exchange), and every output bounded by the largest |v| (a convex
+    combination of the rows of v)."""
     w = W.WORKLOADS[name]
     q, k, v = W.workload_qkv(w)
     txt, img = W.workload_ids(w)
     out = _run_gpu(q, k, v, txt, img)
-    rows = _sample_rows(w.S, w.S_txt, 24, seed=w.index)
-    _compare(out, q, k, v, txt, img, rows=rows)
-    # the smallest workspace (no rotated-K exchange) gives the same bits
     ws = torch.zeros(binding.workspace_bytes(w.S), dtype=torch.uint8, device="cuda")
     assert torch.equal(_run_gpu(q, k, v, txt, img, workspace=ws), out)
-    # every output finite and bounded by the largest |v| (a convex combination)
     assert torch.isfinite(out).all()
     assert out.abs().max().item() <= v.abs().max().item() + 1e-2
+    _compare(out, q, k, v, txt, img)
 
 
 @pytest.mark.parametrize("B,H,S", [(1, 160, 256), (1, 9, 4352), (2, 80, 300)])

@@ -5,7 +5,12 @@ rotation, text tokens with the text weights and the others with the image
 weights ("Diffusers 中 Flux2Transformer2DModel 全面解析", sections
 内部架构双流块与单流块 and 并行化支持; eps 1e-6 from 模型配置参数全解). The
 kernel normalises and rotates in fp32 and rounds to bf16 once; the oracle
-does both in fp64. Bar: max |gpu - oracle| <= 1e-2, mean <= 1e-3.
+does both in fp64. Bar: max |gpu - oracle| <= 1e-2, mean <= 1e-3 over every
+output (the klein-9B and two-reference edit workloads included). Where few
+tokens or large learned weights make the bf16 storage of the normalised,
+rotated rows move the output by more than that bar allows for, the exact
+oracle is compared under the first-order rounding-error model's bound
+(tests/error_model.py).
 """
 import numpy as np
 import pytest
@@ -14,6 +19,7 @@ import torch
 import oracle
 from diffusion_transformer_joint_gb300 import binding, build
 from diffusion_transformer_joint_gb300 import workloads as W
+from tests import error_model as EM
 
 pytestmark = pytest.mark.gpu
 
@@ -81,6 +87,24 @@ def _storage_rounded_reference(q, k, v, txt, img, ws, S_txt):
                                        v.double().numpy(), zero[:S_txt], zero[S_txt:])
 
 
+def _model_sigma(q, k, v, txt, img, ws, S_txt, exact):
+    """sigma of the rounding-error model for the QK-norm path: the exact
+    normalised rows are the rotation's inputs."""
+    c, s = oracle.rope_tables(oracle.joint_ids(txt, img))
+
+    def rows(x, w_txt, w_img):
+        xd = x.double().numpy()
+        n = np.concatenate([oracle.rms_norm(xd[:, :S_txt], w_txt, EPS),
+                            oracle.rms_norm(xd[:, S_txt:], w_img, EPS)], axis=1)
+        return n, oracle.rope_apply(n, c, s)
+
+    qx, qh = rows(q, ws[0], ws[2])
+    kx, kh = rows(k, ws[1], ws[3])
+    return EM.predicted_sigma(qh, kh, v.double().numpy(), exact,
+                              EM.rotated_error_var(qx, c, s, qh),
+                              EM.rotated_error_var(kx, c, s, kh))
+
+
 @pytest.mark.parametrize("B,H,S_txt,S_img", [
     (1, 2, 16, 64),      # tiny workload shape
     (1, 1, 0, 1),        # one token, image only
@@ -113,6 +137,7 @@ def test_qknorm_small_shapes_all_outputs(B, H, S_txt, S_img):
                                           v.float().numpy(), txt, img,
                                           qk_norm=tuple(ws) + (EPS,))
         assert np.abs(got - ref).max() <= MAX_ABS
+        EM.check(got, ref, _model_sigma(q, k, v, txt, img, ws, S_txt, ref), float(v.abs().max()))
 
 
 def test_qknorm_tabled_matches_one_call_and_sharing_is_bit_identical():
@@ -153,13 +178,30 @@ def test_qknorm_unit_weights_undo_a_per_token_scale():
 
 
 @pytest.mark.parametrize("name", ["klein9b", "klein9b_edit2"])
-def test_qknorm_full_workload_sampled_rows(name):
+def test_qknorm_full_workload_all_outputs(name):
     w = W.WORKLOADS[name]
     q, k, v = W.workload_qkv(w)
     txt, img = W.workload_ids(w)
     ws = _weights(500 + w.index)
     out = _run(q, k, v, txt, img, ws)
-    rng = np.random.default_rng(w.index)
-    rows = np.unique(np.concatenate([[0, w.S_txt - 1, w.S_txt, w.S - 1],
-                                     rng.integers(0, w.S, 20)]))
-    _compare(out, q, k, v, txt, img, ws, rows=rows)
+    _compare(out, q, k, v, txt, img, ws)
+
+
+def test_qknorm_peaked_against_exact_oracle():
+    """Learned weights near 3 scale every normalised channel by ~3, so logits
+    have a standard deviation near 9 and few keys carry each row. Compared
+    with the plain oracle of the inputs under the rounding-error model's
+    bound, computed before the output is looked at."""
+    B, H, S_txt, S_img = 1, 2, 33, 484
+    S = S_txt + S_img
+    q = W.normal_bf16((B, S, H, 128), 451)
+    k = W.normal_bf16((B, S, H, 128), 452)
+    v = W.normal_bf16((B, S, H, 128), 453)
+    ids = W.random_ids(S, 454, 0, 600)
+    txt, img = ids[:S_txt], ids[S_txt:]
+    ws = _weights(455, 2.5, 3.5)
+    exact = oracle.joint_rope_attention(q.float().numpy(), k.float().numpy(), v.float().numpy(),
+                                        txt, img, qk_norm=tuple(ws) + (EPS,))
+    sigma = _model_sigma(q, k, v, txt, img, ws, S_txt, exact)
+    out = _run(q, k, v, txt, img, ws)
+    EM.check(out.float().cpu().numpy(), exact, sigma, float(v.abs().max()))
