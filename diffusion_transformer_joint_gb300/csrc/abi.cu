@@ -163,15 +163,16 @@ int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids
   int *status = reinterpret_cast<int *>(ws);
   uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
+  // the table kernel clears the status word; the attention kernel overlaps
+  // its start with it (programmatic dependent launch)
   if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
-                               nullptr, nullptr, table, st) != cudaSuccess)
+                               nullptr, nullptr, table, st, status) != cudaSuccess)
     return FLUX_ERR_CUDA;
   void *krot = used == need ? nullptr : static_cast<void *>(ws + need);
   flux::QkNormArgs nargs{};
   if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot,
-                                   norm_w != nullptr ? &nargs : nullptr, st) != cudaSuccess)
+                                   norm_w != nullptr ? &nargs : nullptr, st, true) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }
@@ -349,10 +350,10 @@ static int extract_call(const void *q, const void *k, const void *v, const int32
   uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
   void *xbuf = ws + flux::kStatusBytes + flux::packed_table_bytes(S, D);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
-  // the table of [txt ; ref ; img]: two launches of the two-segment table kernel
+  // the table of [txt ; ref ; img]: two launches of the two-segment table
+  // kernel, the first of which clears the status word
   if (flux::launch_rope_tables(txt_ids, S_txt, ref_ids, S_ref, pp, flux::TableFormat::kPackedF16,
-                               nullptr, nullptr, table, st) != cudaSuccess ||
+                               nullptr, nullptr, table, st, status) != cudaSuccess ||
       (S_img > 0 &&
        flux::launch_rope_tables(img_ids, S_img, nullptr, 0, pp, flux::TableFormat::kPackedF16,
                                 nullptr, nullptr, table + (S_txt + S_ref) * (D / 2), st) !=
@@ -364,8 +365,8 @@ static int extract_call(const void *q, const void *k, const void *v, const int32
   flux::QkNormArgs nargs{};
   if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, sg, n,
-                                      nullptr, xbuf, norm_w != nullptr ? &nargs : nullptr,
-                                      st) != cudaSuccess)
+                                      nullptr, xbuf, norm_w != nullptr ? &nargs : nullptr, st,
+                                      true) != cudaSuccess)
     return FLUX_ERR_CUDA;
   if (S_ref > 0) {
     // the cache: every key tile was rotated once into the exchange buffer's
@@ -448,9 +449,8 @@ static int cached_call(const void *q, const void *k, const void *v, const int32_
   uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
   void *xbuf = ws + flux::kStatusBytes + flux::packed_table_bytes(S_q, D);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return FLUX_ERR_CUDA;
   if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
-                               nullptr, nullptr, table, st) != cudaSuccess)
+                               nullptr, nullptr, table, st, status) != cudaSuccess)
     return FLUX_ERR_CUDA;
   const flux::AttnSegment all{0, S_q, 0, S_q, 0, S_ref};
   const flux::PreRotatedKV cache{cache_k, cache_v, S_ref};
@@ -458,8 +458,8 @@ static int cached_call(const void *q, const void *k, const void *v, const int32_
   flux::QkNormArgs nargs{};
   if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_attention_segments(q, k, v, out, table, table, status, B, S_q, S_q, H, &all, 1,
-                                      &cache, xbuf, norm_w != nullptr ? &nargs : nullptr,
-                                      st) != cudaSuccess)
+                                      &cache, xbuf, norm_w != nullptr ? &nargs : nullptr, st,
+                                      true) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }

@@ -911,6 +911,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // --------------------------------------------------------- RoPE warps
     reg_dec<kRegsRope>();
+    // everything below reads the table: wait for the kernel that writes it
+    // when this one was launched to overlap it (a no-op otherwise)
+    grid_dep_wait();
     const int u = tid - 384;
     bool ok = true;
     int tuse = 0;   // table-buffer halves consumed so far
@@ -1070,7 +1073,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (tid == 0 && *abort_flag) atomicExch(status, FLUX_ERR_DEVICE_TIMEOUT);
+  if (tid == 0 && *abort_flag) {
+    grid_dep_wait();  // after the table kernel's clear of the same word
+    atomicExch(status, FLUX_ERR_DEVICE_TIMEOUT);
+  }
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
@@ -1167,7 +1173,7 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
                                       const AttnSegment *segs, int n_segs,
                                       const PreRotatedKV *pre, void *xbuf,
-                                      const QkNormArgs *norm, cudaStream_t stream) {
+                                      const QkNormArgs *norm, cudaStream_t stream, bool pdl) {
   if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
   static std::once_flag attr_once[64];
   int dev = 0;
@@ -1255,28 +1261,40 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   const uint16_t *qg = static_cast<const uint16_t *>(q), *kg = static_cast<const uint16_t *>(k);
   uint16_t *og = static_cast<uint16_t *>(out);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  const int n_items = static_cast<int>(items);
+  const uint64_t token = next_launch_token();
   if (norm != nullptr) {
     const QkNorm qn{norm->q_txt, norm->q_img, norm->s_txt, norm->eps};
     const QkNorm kn{norm->k_txt, norm->k_img, norm->s_txt, norm->eps};
-    joint_rope_attention_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(
-        maps, og, status, sg, S_q, S_k, H, static_cast<int>(items), kflags, krot, qrot, qg, kg,
-        table_q, table_k, next_launch_token(), qn, kn);
+    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<true>, maps, og, status, sg, S_q, S_k,
+                           H, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token, qn,
+                           kn);
   } else {
     const QkNorm none{nullptr, nullptr, 0, 0.f};
-    joint_rope_attention_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(
-        maps, og, status, sg, S_q, S_k, H, static_cast<int>(items), kflags, krot, qrot, qg, kg,
-        table_q, table_k, next_launch_token(), none, none);
+    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<false>, maps, og, status, sg, S_q,
+                           S_k, H, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token,
+                           none, none);
   }
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
                                    void *krot_scratch, const QkNormArgs *norm,
-                                   cudaStream_t stream) {
+                                   cudaStream_t stream, bool pdl) {
   const AttnSegment all{0, S, 0, S, 0, 0};
   return launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, &all, 1,
-                                   nullptr, krot_scratch, norm, stream);
+                                   nullptr, krot_scratch, norm, stream, pdl);
 }
 
 }  // namespace flux

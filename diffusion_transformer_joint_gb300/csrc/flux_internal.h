@@ -43,9 +43,13 @@ enum class TableFormat {
 
 // Enqueues the table kernel over the joint id sequence [seg0 ; seg1]. For
 // kPackedF16 the table goes to `packed` ([S, P] uint32) and cos/sin are unused.
+// `clear` (nullable): a device int the kernel sets to 0 (a call's status
+// word). The kernel lets a programmatically dependent launch (an attention
+// kernel launched with pdl) begin as soon as it starts.
 cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *ids1, int64_t S1,
                                const RopePairs &pp, TableFormat fmt, float *cos_out,
-                               float *sin_out, uint32_t *packed, cudaStream_t stream);
+                               float *sin_out, uint32_t *packed, cudaStream_t stream,
+                               int *clear = nullptr);
 
 // Workspace layout of flux_joint_rope_attention: a 256-byte status block,
 // then the packed table [S, D/2] uint32, padded to 256 bytes.
@@ -107,12 +111,17 @@ size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment 
 // K / V [B, S_k, H, 128] bf16; table_q [S_q, 64] and table_k [S_k, 64]
 // packed tables for the rows of Q and of K; xbuf (nullable) the exchange
 // buffer of exchange_bytes(...) bytes, 256-byte aligned.
+// pdl: launch with programmatic stream serialization, so that the kernel's
+// prologue and first Q / K / V copies overlap the table kernel enqueued just
+// before it on `stream` (which must be the previous kernel in the stream);
+// everything that reads the table or the status word waits for it first.
 cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
                                       const uint32_t *table_q, const uint32_t *table_k,
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
                                       const AttnSegment *segs, int n_segs,
                                       const PreRotatedKV *pre, void *xbuf,
-                                      const QkNormArgs *norm, cudaStream_t stream);
+                                      const QkNormArgs *norm, cudaStream_t stream,
+                                      bool pdl = false);
 
 // The driver's cuTensorMapEncodeTiled for the projection's tensor maps,
 // fetched once through the runtime (no -lcuda); NULL when unavailable.
@@ -133,6 +142,6 @@ cudaError_t launch_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
                                    void *krot_scratch, const QkNormArgs *norm,
-                                   cudaStream_t stream);
+                                   cudaStream_t stream, bool pdl = false);
 
 }  // namespace flux

@@ -400,6 +400,17 @@ __device__ __forceinline__ void fence_acq_rel_gpu() {
 }
 // Orders this thread's generic-proxy global accesses with its async-proxy
 // (TMA) ones.
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream still
+// runs; griddepcontrol.wait blocks the calling thread until that kernel has
+// completed and its memory operations are visible (a no-op when the launch
+// had no such dependency). launch_dependents lets the next kernel's launch
+// begin once every block of this kernel has issued it or exited.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }

@@ -21,12 +21,16 @@
 #include <cmath>
 
 #include "flux_internal.h"
+#include "ptx_sm103a.cuh"
 
 namespace flux {
 namespace {
 
 // One block row of threads per token: threadIdx.x walks the pairs,
-// threadIdx.y the tokens of the block; the grid strides over tokens.
+// threadIdx.y the tokens of the block; the grid strides over tokens. The
+// per-pair parameters are staged in shared memory once per block: read from
+// the parameter space with a different pair per lane, every access would be
+// serialised across the warp.
 template <TableFormat kFmt>
 __global__ void __launch_bounds__(256) rope_tables_kernel(const int32_t *__restrict__ ids0,
                                                           int64_t S0,
@@ -34,14 +38,26 @@ __global__ void __launch_bounds__(256) rope_tables_kernel(const int32_t *__restr
                                                           int64_t S, const RopePairs pp,
                                                           float *__restrict__ cos_out,
                                                           float *__restrict__ sin_out,
-                                                          uint32_t *__restrict__ packed) {
+                                                          uint32_t *__restrict__ packed,
+                                                          int *__restrict__ clear) {
+  // the attention kernel after this one may begin launching (it waits for
+  // this grid before it reads the table or the cleared word)
+  grid_dep_launch_dependents();
+  if (clear != nullptr && blockIdx.x == 0 && threadIdx.x == 0 && threadIdx.y == 0) *clear = 0;
+  __shared__ uint64_t turns_q64[kMaxPairs];
+  __shared__ uint8_t axis[kMaxPairs];
   const int P = pp.n_pairs;
+  for (int p = threadIdx.y * blockDim.x + threadIdx.x; p < P; p += blockDim.x * blockDim.y) {
+    turns_q64[p] = pp.turns_q64[p];
+    axis[p] = pp.axis[p];
+  }
+  __syncthreads();
   for (int64_t s = static_cast<int64_t>(blockIdx.x) * blockDim.y + threadIdx.y; s < S;
        s += static_cast<int64_t>(gridDim.x) * blockDim.y) {
     const int32_t *row = (s < S0) ? ids0 + s * pp.n_axes : ids1 + (s - S0) * pp.n_axes;
     for (int p = threadIdx.x; p < P; p += blockDim.x) {
       const uint64_t prod =
-          static_cast<uint64_t>(static_cast<int64_t>(row[pp.axis[p]])) * pp.turns_q64[p];
+          static_cast<uint64_t>(static_cast<int64_t>(row[axis[p]])) * turns_q64[p];
       const int32_t turn_q32 = static_cast<int32_t>(prod >> 32);  // [-1/2, 1/2) turns, Q0.32
       const float two_f = static_cast<float>(turn_q32) * 4.656612873077393e-10f;  // 2^-31
       float sn, cs;
@@ -99,7 +115,8 @@ int make_rope_pairs(const int32_t *axes_dims, int n_axes, double theta, RopePair
 
 cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *ids1, int64_t S1,
                                const RopePairs &pp, TableFormat fmt, float *cos_out,
-                               float *sin_out, uint32_t *packed, cudaStream_t stream) {
+                               float *sin_out, uint32_t *packed, cudaStream_t stream,
+                               int *clear) {
   const int64_t S = S0 + S1;
   const dim3 block(64, 4);
   int64_t blocks = (S + block.y - 1) / block.y;
@@ -109,10 +126,10 @@ cudaError_t launch_rope_tables(const int32_t *ids0, int64_t S0, const int32_t *i
   if (blocks < 1) blocks = 1;
   if (fmt == TableFormat::kF32Pair)
     rope_tables_kernel<TableFormat::kF32Pair><<<static_cast<unsigned>(blocks), block, 0, stream>>>(
-        ids0, S0, ids1, S, pp, cos_out, sin_out, packed);
+        ids0, S0, ids1, S, pp, cos_out, sin_out, packed, clear);
   else
     rope_tables_kernel<TableFormat::kPackedF16><<<static_cast<unsigned>(blocks), block, 0, stream>>>(
-        ids0, S0, ids1, S, pp, cos_out, sin_out, packed);
+        ids0, S0, ids1, S, pp, cos_out, sin_out, packed, clear);
   return cudaGetLastError();
 }
 

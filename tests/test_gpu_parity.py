@@ -244,7 +244,11 @@ def test_peaked_softmax_against_exact_oracle():
                                EM.rotated_error_var(qx, c, s, qh),
                                EM.rotated_error_var(kx, c, s, kh))
     out = _run_gpu(q, k, v, ids[:33], ids[33:])
-    EM.check(out.float().cpu().numpy(), exact, sigma, float(v.abs().max()))
+    got = out.float().cpu().numpy()
+    worst, mean_ratio = EM.check(got, exact, sigma, float(v.abs().max()))
+    print(f"q x 8 vs exact: max err {np.abs(got - exact).max():.3e}, mean "
+          f"{np.abs(got - exact).mean():.3e}, worst element at {worst:.2f} of its bound, "
+          f"mean at {mean_ratio:.2f} of its bound")
     # the fp16 table's own cost against the plain oracle
     c16 = c.astype(np.float16).astype(np.float64)
     s16 = s.astype(np.float16).astype(np.float64)

@@ -204,4 +204,8 @@ def test_qknorm_peaked_against_exact_oracle():
                                         txt, img, qk_norm=tuple(ws) + (EPS,))
     sigma = _model_sigma(q, k, v, txt, img, ws, S_txt, exact)
     out = _run(q, k, v, txt, img, ws)
-    EM.check(out.float().cpu().numpy(), exact, sigma, float(v.abs().max()))
+    got = out.float().cpu().numpy()
+    worst, mean_ratio = EM.check(got, exact, sigma, float(v.abs().max()))
+    print(f"QK norm, weights ~3, vs exact: max err {np.abs(got - exact).max():.3e}, mean "
+          f"{np.abs(got - exact).mean():.3e}, worst element at {worst:.2f} of its bound, "
+          f"mean at {mean_ratio:.2f} of its bound")
