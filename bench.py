@@ -855,6 +855,134 @@ def cpu_report(seconds=3.0):
     return {"cpu_report": report, "kind": "oracle", "dtype": "f64"}
 
 
+# ------------------------------------------- head- and sequence-parallel ranks
+
+
+def run_sharded(args, rank, world, local_rank):
+    """One klein-9B-shaped call split over the ranks (strong scaling: the whole
+    job does one call's work per step).
+
+    heads: rank r attends its contiguous range of heads of the same [B, S, H,
+    128] inputs (flux_joint_rope_attention_heads); nothing moves between ranks.
+    seq: rank r holds the q, k, v rows of its contiguous range of tokens; each
+    step all-gathers K and V (NCCL), then attends its query rows over every
+    key (flux_joint_rope_attention_rows). The gather is inside the step."""
+    import numpy as np
+    import torch
+
+    from diffusion_transformer_joint_gb300 import binding, shard
+    from diffusion_transformer_joint_gb300 import build as cuda_build
+    from diffusion_transformer_joint_gb300 import workloads as W
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if rank == 0 or not os.path.exists(cuda_build.LIB_PATH):
+        cuda_build.build()
+    if dist is not None:
+        dist.barrier()
+    binding.load()
+    w = W.WORKLOADS[args.workload]
+    txt_np, img_np = W.workload_ids(w)
+    ids = torch.from_numpy(np.concatenate([txt_np, img_np])).to(dev)
+    txt_d, img_d = ids[:w.S_txt], ids[w.S_txt:]
+    set_bytes = 3 * w.B * w.S * w.H * w.D * 2
+    n_sets = max(2, -(-2 * L2_BYTES // set_bytes) + 1)
+    stream = torch.cuda.Stream(device=dev)
+    if args.shard == "heads":
+        h0, n = shard.head_range(rank, world, w.H)
+        flops_rank = w.flops * n // w.H
+        sets = []
+        for i in range(n_sets):  # every rank holds the same inputs (one call split by heads)
+            q, k, v = W.workload_qkv(w, seed_offset=17 * i)
+            sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev)))
+        ws = torch.zeros(binding.workspace_shared_bytes(w.B, w.S, n, w.D), dtype=torch.uint8,
+                         device=dev)
+
+        def step(i):
+            q, k, v, out = sets[i % n_sets]
+            binding.joint_rope_attention_heads(q, k, v, txt_d, img_d, h0, n, out=out,
+                                               workspace=ws, stream=stream)
+        part = f"heads {h0}..{h0 + n - 1} of {w.H} on rank {rank}"
+    else:
+        q0, n = shard.seq_range(rank, world, w.S)
+        flops_rank = 4 * w.B * w.H * n * w.S * w.D
+        sets = []
+        for i in range(n_sets):
+            q, k, v = W.workload_qkv(w, seed_offset=17 * i)
+            sets.append(tuple(x[:, q0:q0 + n].contiguous().to(dev) for x in (q, k, v)))
+        k_full = torch.empty((w.B, w.S, w.H, w.D), dtype=torch.bfloat16, device=dev)
+        v_full = torch.empty_like(k_full)
+        out = torch.empty((w.B, n, w.H, w.D), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(binding.rows_workspace_bytes(w.B, n, w.S, w.H, w.D), dtype=torch.uint8,
+                         device=dev)
+
+        def step(i):
+            q, k, v = sets[i % n_sets]
+            with torch.cuda.stream(stream):
+                if dist is not None:
+                    shard.gather_sequence(k, w.S, dist, out=k_full)
+                    shard.gather_sequence(v, w.S, dist, out=v_full)
+                else:
+                    k_full.copy_(k)
+                    v_full.copy_(v)
+            binding.joint_rope_attention_rows(q, q0, k_full, v_full, txt_d, img_d, out=out,
+                                              workspace=ws, stream=stream)
+        part = f"query rows {q0}..{q0 + n - 1} of {w.S} on rank {rank}"
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    stream.synchronize()
+    K = args.steps
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for i in range(K):
+                step(i)
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    if binding.query_status(ws, stream) != 0:
+        raise RuntimeError("device status set during the timed steps")
+    t_max = max_over_ranks(ev0.elapsed_time(ev1), dist, dev)
+    if rank != 0:
+        return None
+    peaks, peak_src = _peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    value = w.flops * K / (t_max * 1e-3) / 1e12  # one call's FLOPs per step, all ranks
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(t_max / K, 4), "higher_is_better": True,
+        "scaling": "strong", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16 q/k/v, FLUX.2 (T,H,W,L) ids)",
+        "config": {
+            "workload": f"{w.name}: B={w.B} H={w.H} S={w.S} ({w.S_txt} text + {w.S_img} image) "
+                        f"head_dim={w.D} axes=(32,32,32,32) theta=2000 non-causal",
+            "B": w.B, "H": w.H, "S": w.S,
+            "parallelism": (f"head parallel x{world}: each rank attends its heads, no "
+                            "collective" if args.shard == "heads" else
+                            f"sequence parallel x{world}: K and V all-gathered every step, "
+                            "each rank attends its query rows over every key"),
+            "rank0": part,
+            "l2": f"inputs rotate over {n_sets} sets",
+            "flops_rank0_per_step": flops_rank,
+        },
+        "pct_peak": round(100.0 * value / world / peak, 2),
+        "clocks": clocks.summary(),
+        "e2e": None,
+        "e2e_note": "end-to-end copies are measured on the replicas line (the default)",
+        "gpu_launches": 2 * K,
+    }
+
+
 def run_reference(args, rank, world):
     """The oracle on the host cores: each step is a bounded sample of the same
     workload; the line carries the same metric and unit as ours."""
@@ -911,11 +1039,29 @@ def main():
                     help="time the fused single-stream QKV+MLP input projection instead")
     ap.add_argument("--qk-norm", action="store_true",
                     help="time the entry with the fused QK RMS normalisation before RoPE")
+    ap.add_argument("--shard", choices=("replicas", "heads", "seq"), default="replicas",
+                    help="replicas: every rank runs its own call (weak scaling, the default); "
+                         "heads / seq: one call split over the ranks by heads or by tokens "
+                         "(strong scaling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # not started by a launcher: start one rank per GPU on this node
+        import socket
+        import subprocess
+
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr", "127.0.0.1",
+               f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+        sys.exit(subprocess.run(cmd).returncode)
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE is {world}")
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.cpu_report:
@@ -931,6 +1077,8 @@ def main():
             dist.init_process_group("nccl")
         if args.proj:
             line = run_proj(args, rank, world, local_rank)
+        elif args.shard != "replicas":
+            line = run_sharded(args, rank, world, local_rank)
         elif args.kv_mode is not None:
             if args.workload == "klein9b":
                 args.workload = "klein9b_edit2"

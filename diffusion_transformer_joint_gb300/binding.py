@@ -25,6 +25,8 @@ STATUS = {
 EXPORTS = ("flux_rope_tables", "flux_rope_tables_packed", "flux_joint_rope_attention_workspace",
            "flux_joint_rope_attention_krot_bytes", "flux_joint_rope_attention_workspace_shared",
            "flux_joint_rope_attention", "flux_joint_rope_attention_tabled",
+           "flux_joint_rope_attention_heads", "flux_joint_rope_attention_rows",
+           "flux_joint_rope_attention_rows_workspace",
            "flux_joint_qknorm_rope_attention", "flux_joint_qknorm_rope_attention_tabled",
            "flux_joint_rope_attention_extract_workspace", "flux_joint_rope_attention_extract",
            "flux_joint_rope_attention_cached_workspace", "flux_joint_rope_attention_cached",
@@ -74,6 +76,14 @@ def load(path: str | None = None):
             lib.flux_joint_rope_attention.restype = I32
             lib.flux_joint_rope_attention_tabled.argtypes = [V, V, V, V, I32, I64, I32, I32, V,
                                                              V, V, SZ, V]
+            lib.flux_joint_rope_attention_heads.argtypes = [V, V, V, V, I64, V, I64, I32, I32,
+                                                            I32, I32, I32, V, I32, D, V, V, SZ, V]
+            lib.flux_joint_rope_attention_heads.restype = I32
+            lib.flux_joint_rope_attention_rows.argtypes = [V, I64, I64, V, V, V, I64, V, I64, I32,
+                                                           I32, I32, V, I32, D, V, V, SZ, V]
+            lib.flux_joint_rope_attention_rows.restype = I32
+            lib.flux_joint_rope_attention_rows_workspace.argtypes = [I32, I64, I64, I32, I32]
+            lib.flux_joint_rope_attention_rows_workspace.restype = SZ
             lib.flux_joint_rope_attention_tabled.restype = I32
             F = ctypes.c_float
             lib.flux_joint_qknorm_rope_attention.argtypes = [
@@ -306,6 +316,99 @@ def joint_rope_attention(q, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=T
         name = "flux_joint_qknorm_rope_attention"
     if rc != 0:
         raise FluxError(name, rc, lib)
+    return out
+
+
+def _check_ids(txt_ids, img_ids, n_axes):
+    import torch
+
+    for name, t in (("txt_ids", txt_ids), ("img_ids", img_ids)):
+        if t is not None and t.numel() > 0:
+            _need_cuda(name, t, torch.int32)
+            _need_ids(name, t, n_axes)
+    return (0 if txt_ids is None else int(txt_ids.shape[0]),
+            0 if img_ids is None else int(img_ids.shape[0]))
+
+
+def joint_rope_attention_heads(q, k, v, txt_ids, img_ids, h0, n_heads, axes_dims=AXES_DIMS,
+                               theta=THETA, out=None, workspace=None, stream=None, share_k=True):
+    """joint_rope_attention over heads h0 .. h0 + n_heads - 1 of the [B, S, H, 128]
+    tensors q, k, v (a tensor-parallel rank's heads); only those heads of
+    ``out`` are written (it is allocated, and left uninitialised elsewhere,
+    when None)."""
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+    B, S, H, D = q.shape
+    _need_shape("k", k, q.shape)
+    _need_shape("v", v, q.shape)
+    S_txt, S_img = _check_ids(txt_ids, img_ids, len(axes_dims))
+    if S_txt + S_img != S:
+        raise ValueError(f"the ids give {S_txt} + {S_img} tokens, q has {S}")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        _need_shape("out", out, q.shape)
+    if workspace is None:
+        n = workspace_shared_bytes(B, S, int(n_heads), D) if share_k else 0
+        workspace = torch.empty(max(n or workspace_bytes(S, D), 256), dtype=torch.uint8,
+                                device=q.device)
+    else:
+        _need_cuda("workspace", workspace, torch.uint8)
+    axes, n = _axes_array(axes_dims)
+    rc = lib.flux_joint_rope_attention_heads(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B, H, int(h0),
+        int(n_heads), D, axes, n, float(theta), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention_heads", rc, lib)
+    return out
+
+
+def rows_workspace_bytes(B: int, S_q: int, S: int, H: int, D: int = 128) -> int:
+    """Workspace of joint_rope_attention_rows with the exchange buffer."""
+    return int(load().flux_joint_rope_attention_rows_workspace(int(B), int(S_q), int(S), int(H),
+                                                               int(D)))
+
+
+def joint_rope_attention_rows(q, q0, k, v, txt_ids, img_ids, axes_dims=AXES_DIMS, theta=THETA,
+                              out=None, workspace=None, stream=None, share_k=True):
+    """The attention of query tokens q0 .. q0 + S_q - 1 (q: bf16 [B, S_q, H, 128])
+    over every token's key and value (k, v: [B, S, H, 128]); txt_ids / img_ids
+    are the ids of the whole sequence. Returns out [B, S_q, H, 128]."""
+    import torch
+
+    lib = load()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need_cuda(name, t, torch.bfloat16)
+    B, S_q, H, D = q.shape
+    S = k.shape[1]
+    _need_shape("k", k, (B, S, H, D))
+    _need_shape("v", v, (B, S, H, D))
+    S_txt, S_img = _check_ids(txt_ids, img_ids, len(axes_dims))
+    if S_txt + S_img != S:
+        raise ValueError(f"the ids give {S_txt} + {S_img} tokens, k has {S}")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _need_cuda("out", out, torch.bfloat16)
+        _need_shape("out", out, q.shape)
+    if workspace is None:
+        n = rows_workspace_bytes(B, S_q, S, H, D) if share_k else 0
+        workspace = torch.empty(max(n or workspace_bytes(S, D), 256), dtype=torch.uint8,
+                                device=q.device)
+    else:
+        _need_cuda("workspace", workspace, torch.uint8)
+    axes, n = _axes_array(axes_dims)
+    rc = lib.flux_joint_rope_attention_rows(
+        _ptr(q), int(q0), S_q, _ptr(k), _ptr(v), _ptr(txt_ids), S_txt, _ptr(img_ids), S_img, B,
+        H, D, axes, n, float(theta), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream))
+    if rc != 0:
+        raise FluxError("flux_joint_rope_attention_rows", rc, lib)
     return out
 
 

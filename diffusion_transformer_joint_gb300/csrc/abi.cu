@@ -120,10 +120,12 @@ int check_norm(const float *const w[4], float eps, int64_t S_txt, int64_t S) {
   return FLUX_OK;
 }
 
+// The one-call attention over heads h0 .. h0 + Hl - 1 of [B, S, H, D] tensors.
 int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids, int64_t S_txt,
              const int32_t *img_ids, int64_t S_img, int B, int H, int D,
              const int32_t *axes_dims, int n_axes, double theta, const float *const norm_w[4],
-             float eps, void *out, void *workspace, size_t workspace_bytes, void *stream) {
+             float eps, void *out, void *workspace, size_t workspace_bytes, void *stream,
+             int h0, int Hl) {
   if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
     return FLUX_ERR_NULL;
   if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr)) return FLUX_ERR_NULL;
@@ -131,6 +133,7 @@ int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids
   const int64_t S = S_txt + S_img;
   if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
     return FLUX_ERR_SHAPE;
+  if (h0 < 0 || Hl < 1 || h0 > H - Hl) return FLUX_ERR_SHAPE;
   if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
   flux::RopePairs pp;
   const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
@@ -150,8 +153,8 @@ int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids
   if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < need)
     return FLUX_ERR_WORKSPACE;
-  // a workspace large enough for the exchange buffer enables it
-  const size_t need_shared = flux_joint_rope_attention_workspace_shared(B, S, H, D);
+  // a workspace large enough for the exchange buffer (of the Hl heads) enables it
+  const size_t need_shared = flux_joint_rope_attention_workspace_shared(B, S, Hl, D);
   const size_t used = (need_shared != 0 && workspace_bytes >= need_shared) ? need_shared : need;
   if (overlaps(workspace, used, q, tensor_bytes) || overlaps(workspace, used, k, tensor_bytes) ||
       overlaps(workspace, used, v, tensor_bytes) || overlaps(workspace, used, out, tensor_bytes))
@@ -172,7 +175,8 @@ int one_call(const void *q, const void *k, const void *v, const int32_t *txt_ids
   flux::QkNormArgs nargs{};
   if (norm_w != nullptr) nargs = {norm_w[0], norm_w[1], norm_w[2], norm_w[3], S_txt, eps};
   if (flux::launch_joint_attention(q, k, v, out, table, status, B, S, H, krot,
-                                   norm_w != nullptr ? &nargs : nullptr, st, true) != cudaSuccess)
+                                   norm_w != nullptr ? &nargs : nullptr, st, true, h0,
+                                   Hl) != cudaSuccess)
     return FLUX_ERR_CUDA;
   return FLUX_OK;
 }
@@ -228,7 +232,17 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
                               int n_axes, double theta, void *out, void *workspace,
                               size_t workspace_bytes, void *stream) {
   return one_call(q, k, v, txt_ids, S_txt, img_ids, S_img, B, H, D, axes_dims, n_axes, theta,
-                  nullptr, 0.f, out, workspace, workspace_bytes, stream);
+                  nullptr, 0.f, out, workspace, workspace_bytes, stream, 0, H);
+}
+
+int flux_joint_rope_attention_heads(const void *q, const void *k, const void *v,
+                                    const int32_t *txt_ids, int64_t S_txt,
+                                    const int32_t *img_ids, int64_t S_img, int B, int H, int h0,
+                                    int H_local, int D, const int32_t *axes_dims, int n_axes,
+                                    double theta, void *out, void *workspace,
+                                    size_t workspace_bytes, void *stream) {
+  return one_call(q, k, v, txt_ids, S_txt, img_ids, S_img, B, H, D, axes_dims, n_axes, theta,
+                  nullptr, 0.f, out, workspace, workspace_bytes, stream, h0, H_local);
 }
 
 int flux_joint_qknorm_rope_attention(const void *q, const void *k, const void *v,
@@ -241,7 +255,7 @@ int flux_joint_qknorm_rope_attention(const void *q, const void *k, const void *v
                                      void *stream) {
   const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
   return one_call(q, k, v, txt_ids, S_txt, img_ids, S_img, B, H, D, axes_dims, n_axes, theta, w,
-                  eps, out, workspace, workspace_bytes, stream);
+                  eps, out, workspace, workspace_bytes, stream, 0, H);
 }
 
 int flux_joint_rope_attention_tabled(const void *q, const void *k, const void *v,
@@ -262,6 +276,72 @@ int flux_joint_qknorm_rope_attention_tabled(const void *q, const void *k, const 
   const float *const w[4] = {q_norm_txt, k_norm_txt, q_norm_img, k_norm_img};
   return tabled(q, k, v, table, B, S, H, D, S_txt, w, eps, out, status, krot_scratch, krot_bytes,
                 stream);
+}
+
+// ---------------------------------------------- a slice of the query rows
+
+size_t flux_joint_rope_attention_rows_workspace(int B, int64_t S_q, int64_t S, int H, int D) {
+  if (D != 128 || B < 1 || H < 1 || S_q < 1 || S < S_q || S > 0x7FFFFFFFLL || B > 65535 ||
+      H > 65535 || static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL)
+    return 0;
+  const flux::AttnSegment seg{0, S_q, 0, S, 0, 0};
+  return flux::kStatusBytes + flux::packed_table_bytes(S, D) +
+         flux::exchange_bytes(B, S_q, S, H, &seg, 1);
+}
+
+int flux_joint_rope_attention_rows(const void *q, int64_t q0, int64_t S_q, const void *k,
+                                   const void *v, const int32_t *txt_ids, int64_t S_txt,
+                                   const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                   const int32_t *axes_dims, int n_axes, double theta, void *out,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr || axes_dims == nullptr)
+    return FLUX_ERR_NULL;
+  if ((S_txt > 0 && txt_ids == nullptr) || (S_img > 0 && img_ids == nullptr)) return FLUX_ERR_NULL;
+  if (S_txt < 0 || S_img < 0 || S_txt > 0x7FFFFFFFLL || S_img > 0x7FFFFFFFLL)
+    return FLUX_ERR_SHAPE;
+  const int64_t S = S_txt + S_img;
+  if (D != 128 || B < 1 || H < 1 || S < 1 || S > 0x7FFFFFFFLL || B > 65535 || H > 65535)
+    return FLUX_ERR_SHAPE;
+  if (q0 < 0 || S_q < 1 || q0 > S - S_q) return FLUX_ERR_SHAPE;
+  if (static_cast<int64_t>(B) * H * ((S + 127) / 128) > 0x7FFFFFFFLL) return FLUX_ERR_SHAPE;
+  flux::RopePairs pp;
+  const int rc = flux::make_rope_pairs(axes_dims, n_axes, theta, &pp);
+  if (rc != FLUX_OK) return rc;
+  if (2 * pp.n_pairs != D) return FLUX_ERR_AXES;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FLUX_ERR_ALIGN;
+  const size_t row = static_cast<size_t>(H) * D * 2;
+  const size_t qb = static_cast<size_t>(B) * static_cast<size_t>(S_q) * row;
+  const size_t kb = static_cast<size_t>(B) * static_cast<size_t>(S) * row;
+  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb))
+    return FLUX_ERR_ALIAS;
+  const size_t need = flux_joint_rope_attention_workspace(S, D);
+  if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < need)
+    return FLUX_ERR_WORKSPACE;
+  const size_t need_shared = flux_joint_rope_attention_rows_workspace(B, S_q, S, H, D);
+  const size_t used = (need_shared != 0 && workspace_bytes >= need_shared) ? need_shared : need;
+  if (overlaps(workspace, used, q, qb) || overlaps(workspace, used, k, kb) ||
+      overlaps(workspace, used, v, kb) || overlaps(workspace, used, out, qb))
+    return FLUX_ERR_ALIAS;
+  const int dc = check_device();
+  if (dc != FLUX_OK) return dc;
+
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int *status = reinterpret_cast<int *>(ws);
+  uint32_t *table = reinterpret_cast<uint32_t *>(ws + flux::kStatusBytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (flux::launch_rope_tables(txt_ids, S_txt, img_ids, S_img, pp, flux::TableFormat::kPackedF16,
+                               nullptr, nullptr, table, st, status) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  // queries: rows q0 .. q0 + S_q - 1 of the joint sequence, whose table rows
+  // start q0 rows into the table; keys: every token
+  const flux::AttnSegment seg{0, S_q, 0, S, 0, 0};
+  void *xbuf = used == need ? nullptr : static_cast<void *>(ws + need);
+  if (flux::launch_attention_segments(q, k, v, out, table + q0 * (D / 2), table, status, B, S_q,
+                                      S, H, &seg, 1, nullptr, xbuf, nullptr, st,
+                                      true) != cudaSuccess)
+    return FLUX_ERR_CUDA;
+  return FLUX_OK;
 }
 
 // ---------------------------------------------- reference-image KV modes

@@ -276,7 +276,8 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
 
 // 128 RoPE threads rotate `nrows` rows of one head from global memory to
 // global memory: src / dst point at the first row's channel 0, rows are
-// row_stride elements apart, `tab` at the first row's packed table row. Thread
+// src_stride / dst_stride elements apart, `tab` at the first row's packed
+// table row. Thread
 // u owns 16-byte chunk u & 15 of rows (u >> 4) + 8 i, the row-to-thread map of
 // rotate_half, so RoPE warp w writes the rows r with r mod 8 in {2w, 2w+1}.
 // With kNorm the rows (token tok0 + r) are RMS-normalised first; every lane
@@ -284,8 +285,8 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
 template <bool kNorm>
 __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t *dst,
                                                    const uint32_t *tab, int nrows,
-                                                   int64_t row_stride, int u, const QkNorm &nm,
-                                                   int64_t tok0) {
+                                                   int64_t src_stride, int64_t dst_stride, int u,
+                                                   const QkNorm &nm, int64_t tok0) {
   const int c16 = u & 15;
   const int rsub = u >> 4;
   const NormW nw = kNorm ? load_norm_w(nm, c16) : NormW{};
@@ -298,7 +299,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
       w[i] = make_uint4(0u, 0u, 0u, 0u);
       cs[i] = make_uint4(0u, 0u, 0u, 0u);
       if (r < nrows) {
-        w[i] = ld_global_nc_v4(src + r * row_stride + c16 * 8);
+        w[i] = ld_global_nc_v4(src + r * src_stride + c16 * 8);
         cs[i] = ld_global_nc_v4(tab + static_cast<int64_t>(r) * kPairs + c16 * 4);
       }
     }
@@ -306,7 +307,7 @@ __device__ __forceinline__ void rotate_rows_global(const uint16_t *src, uint16_t
     for (int i = 0; i < 2; ++i) {
       const int r = rsub + 8 * (i0 + i);
       const uint4 o = rope_chunk<kNorm>(w[i], cs[i], nm, tok0 + r, nw);
-      if (r < nrows) st_global_v4(dst + r * row_stride + c16 * 8, o);
+      if (r < nrows) st_global_v4(dst + r * dst_stride + c16 * 8, o);
     }
   }
 }
@@ -317,14 +318,16 @@ struct Maps {
   CUtensorMap q, k, v, out, krot, qrot, table_q, table_k, kpre, vpre;
 };
 
-// A work item: batch b, head h, the 256 query rows from m0 (rows of Q / out
+// A work item: batch b, head h of Q / K / V / out (hx: its index among the
+// launch's heads, which lay out the exchange buffer), the 256 query rows from
+// m0 (rows of Q / out
 // at or past q_hi belong to another segment: computed, never stored), its key
 // range: rows [k_lo, k_hi) of K / V in n_main 128-key tiles, then rows
 // [0, n_pre) of the pre-rotated K / V in the remaining tiles of n_tiles, all
 // walked from tile j0; and the publication flags of the n_main tiles for
 // (b, h) ([n_main][4]; null without the exchange buffer).
 struct Item {
-  int b, h, n_tiles, n_main, j0;
+  int b, h, hx, n_tiles, n_main, j0;
   int64_t m0, q_hi, k_lo, k_hi, n_pre;
   uint64_t *flags;
 };
@@ -375,7 +378,8 @@ template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ outg,
                                 int *__restrict__ status,
-                                const Segs sg, int64_t S_q, int64_t S_k, int H, int n_items,
+                                const Segs sg, int64_t S_q, int64_t S_k, int H, int h0, int Hl,
+                                int n_items,
                                 uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
                                 uint16_t *__restrict__ qrot, const uint16_t *__restrict__ qg,
                                 const uint16_t *__restrict__ kg,
@@ -394,7 +398,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // token strides (elements) of Q / K / V / out (all H heads) and of the
+  // exchange buffer (the launch's Hl heads h0 .. h0 + Hl - 1)
   const int64_t row_stride = static_cast<int64_t>(H) * kD;
+  const int64_t xrow_stride = static_cast<int64_t>(Hl) * kD;
   const bool share = kflags != nullptr;
   // Work items: segment by segment, (batch, head, 256-row block) with the row
   // block fastest, handed out round robin, so CTAs running at the same time
@@ -411,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nrb = sg.n_rb[g];
     const int rb = local % nrb;
     const int bh = local / nrb;
-    it.h = bh % H;
-    it.b = bh / H;
+    it.hx = bh % Hl;
+    it.h = h0 + it.hx;
+    it.b = bh / Hl;
     it.m0 = sg.q_lo[g] + static_cast<int64_t>(rb) * kRowsPerCta;
     it.q_hi = sg.q_hi[g];
     it.k_lo = sg.k_lo[g];
@@ -422,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     it.n_pre = sg.n_pre[g];
     it.j0 = static_cast<int>((static_cast<int64_t>(rb) * it.n_tiles) / nrb);
     it.flags = share ? kflags + sg.flag_off[g] +
-                           (static_cast<int64_t>(it.b) * H + it.h) * it.n_main * 4
+                           (static_cast<int64_t>(it.b) * Hl + it.hx) * it.n_main * 4
                      : nullptr;
     return it;
   };
@@ -517,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t last_k_full = 0, last_k_par = 0;
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++k) {
         const Item it = info(item);
-        const int b = it.b, h = it.h, m0 = static_cast<int>(it.m0);
+        const int b = it.b, h = it.h, hx = it.hx, m0 = static_cast<int>(it.m0);
         const int next = item + static_cast<int>(gridDim.x);
         // the previous item's S MMAs no longer read the Q buffers
         if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
@@ -534,8 +542,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
           for (int t = 0; t < kQTiles; ++t) {
             const uint32_t dst = sbase + kOffQ + t * kTileBytes;
-            tma_load_4d(dst, &maps.qrot, bar(kBarQFull), 0, h, m0 + t * kBM, b);
-            tma_load_4d(dst + kBlockBytes, &maps.qrot, bar(kBarQFull), 64, h, m0 + t * kBM, b);
+            tma_load_4d(dst, &maps.qrot, bar(kBarQFull), 0, hx, m0 + t * kBM, b);
+            tma_load_4d(dst + kBlockBytes, &maps.qrot, bar(kBarQFull), 64, hx, m0 + t * kBM, b);
           }
           mbar_arrive_n(bar(kBarQFull), 3);
         } else {
@@ -605,9 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_k_full |= 1u << s;
             last_k_par = (last_k_par & ~(1u << s)) | ((use & 1u) << s);
             const CUtensorMap *src = pre ? &maps.kpre : &maps.krot;
+            const int hs = pre ? h : hx;  // the cache has all H heads
             mbar_arrive_expect_tx(bar(kBarKFull + s), kTileBytes);
-            tma_load_4d(dst, src, bar(kBarKFull + s), 0, h, krow, b);
-            tma_load_4d(dst + kBlockBytes, src, bar(kBarKFull + s), 64, h, krow, b);
+            tma_load_4d(dst, src, bar(kBarKFull + s), 0, hs, krow, b);
+            tma_load_4d(dst + kBlockBytes, src, bar(kBarKFull + s), 64, hs, krow, b);
             mbar_arrive_n(bar(kBarKFull + s), 3);
           } else {
             const uint32_t par = (raw_par >> s) & 1u;
@@ -947,7 +956,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return;
         if (grow != nullptr)
           rotate_half<kNorm, true>(tile, sbase + kOffT, half, u, nm, tok0, rows_valid, grow,
-                                   row_stride);
+                                   xrow_stride);
         else
           rotate_half<kNorm, false>(tile, sbase + kOffT, half, u, nm, tok0, rows_valid, nullptr, 0);
         warp_arrive(bar(kBarTEmpty), lane);
@@ -975,19 +984,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tok0 = nx.m0 + c * 64;
           n_rows = S_q;
           src = qg + ((static_cast<int64_t>(nx.b) * S_q + tok0) * H + nx.h) * kD;
-          dst = qrot + ((static_cast<int64_t>(nx.b) * S_q + tok0) * H + nx.h) * kD;
+          dst = qrot + ((static_cast<int64_t>(nx.b) * S_q + tok0) * Hl + nx.hx) * kD;
           tab = tabq;
         } else {
           tok0 = tile_row(nx, tile_at(nx, kt)) + ((c - 4) & 1) * 64;
           n_rows = S_k;
           src = kg + ((static_cast<int64_t>(nx.b) * S_k + tok0) * H + nx.h) * kD;
-          dst = krot + ((static_cast<int64_t>(nx.b) * S_k + tok0) * H + nx.h) * kD;
+          dst = krot + ((static_cast<int64_t>(nx.b) * S_k + tok0) * Hl + nx.hx) * kD;
           tab = tabk;
         }
         const int nrows = static_cast<int>(n_rows - tok0 < 64 ? (n_rows - tok0 > 0 ? n_rows - tok0 : 0) : 64);
         if (nrows > 0)
-          rotate_rows_global<kNorm>(src, dst, tab + tok0 * kPairs, nrows, row_stride, u,
-                                    c < 4 ? qn : kn, tok0);
+          rotate_rows_global<kNorm>(src, dst, tab + tok0 * kPairs, nrows, row_stride, xrow_stride,
+                                    u, c < 4 ? qn : kn, tok0);
         fence_proxy_async_global();  // read by TMA copies
         if (c >= 4 && ((c - 4) & 1) == 1) {
           // publish as the in-place path does: this warp's rows, then its flag
@@ -1046,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
       uint16_t *grow =
-          share ? krot + ((static_cast<int64_t>(it.b) * S_k + tok0) * H + it.h) * kD : nullptr;
+          share ? krot + ((static_cast<int64_t>(it.b) * S_k + tok0) * Hl + it.hx) * kD : nullptr;
       rotate_tile(sbase + kOffK + s * kTileBytes, tok0, S_k, grow, kn, &maps.table_k);
       if (!ok) break;
       fence_proxy_async_smem();
@@ -1173,8 +1182,11 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
                                       const AttnSegment *segs, int n_segs,
                                       const PreRotatedKV *pre, void *xbuf,
-                                      const QkNormArgs *norm, cudaStream_t stream, bool pdl) {
+                                      const QkNormArgs *norm, cudaStream_t stream, bool pdl,
+                                      int h0, int Hl) {
   if (n_segs < 1 || n_segs > kMaxSegments) return cudaErrorInvalidValue;
+  if (Hl == 0) Hl = H;
+  if (h0 < 0 || Hl < 1 || h0 > H - Hl) return cudaErrorInvalidValue;
   static std::once_flag attr_once[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1218,7 +1230,7 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     for (int g = 0; g < n_segs; ++g)
       if (segs[g].key_range == r) {
         range_off[r] = off;
-        off += static_cast<int64_t>(B) * H * ((segs[g].k_hi - segs[g].k_lo + kBN - 1) / kBN) * 4;
+        off += static_cast<int64_t>(B) * Hl * ((segs[g].k_hi - segs[g].k_lo + kBN - 1) / kBN) * 4;
         break;
       }
   }
@@ -1237,7 +1249,7 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     sg.n_pre[g] = a.n_pre;
     sg.n_tiles[g] = sg.n_main[g] + static_cast<int>((a.n_pre + kBN - 1) / kBN);
     sg.flag_off[g] = range_off[a.key_range];
-    items += static_cast<int64_t>(B) * H * (a.q_hi > a.q_lo ? sg.n_rb[g] : 0);
+    items += static_cast<int64_t>(B) * Hl * (a.q_hi > a.q_lo ? sg.n_rb[g] : 0);
     if (items > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   }
   sg.first_item[n_segs] = static_cast<int>(items);
@@ -1248,8 +1260,8 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     const size_t flags = (static_cast<size_t>(off) * sizeof(uint64_t) + 255) & ~static_cast<size_t>(255);
     kflags = static_cast<uint64_t *>(xbuf);
     krot = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(xbuf) + flags);
-    qrot = krot + static_cast<size_t>(B) * static_cast<size_t>(S_k) * H * kD;
-    if (!make_head_map(&maps.krot, krot, B, S_k, H) || !make_head_map(&maps.qrot, qrot, B, S_q, H))
+    qrot = krot + static_cast<size_t>(B) * static_cast<size_t>(S_k) * Hl * kD;
+    if (!make_head_map(&maps.krot, krot, B, S_k, Hl) || !make_head_map(&maps.qrot, qrot, B, S_q, Hl))
       return cudaErrorInvalidValue;
   } else {
     maps.krot = maps.k;  // never read
@@ -1277,13 +1289,13 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
     const QkNorm qn{norm->q_txt, norm->q_img, norm->s_txt, norm->eps};
     const QkNorm kn{norm->k_txt, norm->k_img, norm->s_txt, norm->eps};
     e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<true>, maps, og, status, sg, S_q, S_k,
-                           H, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token, qn,
-                           kn);
+                           H, h0, Hl, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token,
+                           qn, kn);
   } else {
     const QkNorm none{nullptr, nullptr, 0, 0.f};
     e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<false>, maps, og, status, sg, S_q,
-                           S_k, H, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token,
-                           none, none);
+                           S_k, H, h0, Hl, n_items, kflags, krot, qrot, qg, kg, table_q, table_k,
+                           token, none, none);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -1291,10 +1303,10 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
                                    void *krot_scratch, const QkNormArgs *norm,
-                                   cudaStream_t stream, bool pdl) {
+                                   cudaStream_t stream, bool pdl, int h0, int Hl) {
   const AttnSegment all{0, S, 0, S, 0, 0};
   return launch_attention_segments(q, k, v, out, table, table, status, B, S, S, H, &all, 1,
-                                   nullptr, krot_scratch, norm, stream, pdl);
+                                   nullptr, krot_scratch, norm, stream, pdl, h0, Hl);
 }
 
 }  // namespace flux

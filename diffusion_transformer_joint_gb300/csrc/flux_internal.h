@@ -115,13 +115,16 @@ size_t exchange_bytes(int B, int64_t S_q, int64_t S_k, int H, const AttnSegment 
 // prologue and first Q / K / V copies overlap the table kernel enqueued just
 // before it on `stream` (which must be the previous kernel in the stream);
 // everything that reads the table or the status word waits for it first.
+// h0, Hl: attend only heads h0 .. h0 + Hl - 1 of the H heads of Q / K / V /
+// out (Hl 0: all H heads); the exchange buffer is laid out for the Hl heads
+// (exchange_bytes with H = Hl).
 cudaError_t launch_attention_segments(const void *q, const void *k, const void *v, void *out,
                                       const uint32_t *table_q, const uint32_t *table_k,
                                       int *status, int B, int64_t S_q, int64_t S_k, int H,
                                       const AttnSegment *segs, int n_segs,
                                       const PreRotatedKV *pre, void *xbuf,
                                       const QkNormArgs *norm, cudaStream_t stream,
-                                      bool pdl = false);
+                                      bool pdl = false, int h0 = 0, int Hl = 0);
 
 // The driver's cuTensorMapEncodeTiled for the projection's tensor maps,
 // fetched once through the runtime (no -lcuda); NULL when unavailable.
@@ -142,6 +145,7 @@ cudaError_t launch_qkv_mlp_proj(const void *x, const void *w, int64_t M, int dim
 cudaError_t launch_joint_attention(const void *q, const void *k, const void *v, void *out,
                                    const uint32_t *table, int *status, int B, int64_t S, int H,
                                    void *krot_scratch, const QkNormArgs *norm,
-                                   cudaStream_t stream, bool pdl = false);
+                                   cudaStream_t stream, bool pdl = false, int h0 = 0,
+                                   int Hl = 0);
 
 }  // namespace flux

@@ -22,8 +22,10 @@
  *     softmax(Q K^T / sqrt(d_k)) V with d_k the head size).
  *
  * Entry points: the RoPE tables (fp32 and packed); the joint attention in one
- * call (tables + attention) or with a caller-built table; both with the QK
- * RMS normalisation fused in front of the rotation; the reference-image KV
+ * call (tables + attention) or with a caller-built table, both also with the
+ * QK RMS normalisation fused in front of the rotation; the one-call attention
+ * over a range of heads or over a slice of the query rows (for tensor- and
+ * sequence-parallel callers); the reference-image KV
  * modes (extract, cached); and the single-stream block's fused input
  * projection (Q, K, V and the SwiGLU-activated MLP input from one GEMM), the
  * producer of the attention's inputs.
@@ -172,6 +174,62 @@ int flux_joint_rope_attention(const void *q, const void *k, const void *v,
                               const int32_t *img_ids, int64_t S_img, int B, int H, int D,
                               const int32_t *axes_dims, int n_axes, double theta, void *out,
                               void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * flux_joint_rope_attention_heads: flux_joint_rope_attention restricted to
+ * the heads h0 .. h0 + H_local - 1 of [B, S, H, D] tensors, for
+ * tensor-parallel callers ("Diffusers 中 Flux2Transformer2DModel 全面解析",
+ * section 并行化支持: Q, K and V are projected column-wise, so each rank owns
+ * a contiguous range of heads and attention needs no exchange between ranks).
+ *
+ *   q, k, v, out   the full [B, S, H, D] tensors (token stride H * D); only the
+ *                  rows of heads h0 .. h0 + H_local - 1 are read or written,
+ *                  the other heads of out are left untouched.
+ *   h0, H_local    0 <= h0, H_local >= 1, h0 + H_local <= H (else FLUX_ERR_SHAPE).
+ *   workspace      >= flux_joint_rope_attention_workspace(S, D) bytes; with at
+ *                  least flux_joint_rope_attention_workspace_shared(B, S,
+ *                  H_local, D) bytes the exchange buffer (sized for the H_local
+ *                  heads) is used.
+ * Everything else as flux_joint_rope_attention, whose output for these heads
+ * it reproduces bit for bit.
+ */
+int flux_joint_rope_attention_heads(const void *q, const void *k, const void *v,
+                                    const int32_t *txt_ids, int64_t S_txt,
+                                    const int32_t *img_ids, int64_t S_img, int B, int H, int h0,
+                                    int H_local, int D, const int32_t *axes_dims, int n_axes,
+                                    double theta, void *out, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
+/*
+ * flux_joint_rope_attention_rows: the joint attention of a contiguous slice of
+ * the query tokens over every key, for sequence-parallel callers ("Diffusers
+ * 中 Flux2Transformer2DModel 全面解析", section 并行化支持: the context-parallel
+ * plan splits the sequence dimension; each rank keeps its query rows and needs
+ * every key and value, which the caller gathers before this call).
+ *
+ *   q          device, bf16 [B, S_q, H, D]: the query rows of joint tokens
+ *              q0 .. q0 + S_q - 1 of the sequence [txt ; img].
+ *   q0, S_q    0 <= q0, S_q >= 1, q0 + S_q <= S = S_txt + S_img.
+ *   k, v       device, bf16 [B, S, H, D]: every token's key and value.
+ *   txt_ids, img_ids  the ids of the whole sequence, as flux_joint_rope_attention.
+ *   out        device, bf16 [B, S_q, H, D]: the output rows of those tokens.
+ *   workspace  >= flux_joint_rope_attention_workspace(S, D) bytes (status word
+ *              and the table of all S tokens); with at least
+ *              flux_joint_rope_attention_rows_workspace(B, S_q, S, H, D) bytes
+ *              its tail serves as the exchange buffer.
+ * Everything else as flux_joint_rope_attention. The query rows are processed
+ * in their own 256-row blocks, so the summation order over keys may differ
+ * from a call over the whole sequence (the result agrees to rounding).
+ */
+int flux_joint_rope_attention_rows(const void *q, int64_t q0, int64_t S_q, const void *k,
+                                   const void *v, const int32_t *txt_ids, int64_t S_txt,
+                                   const int32_t *img_ids, int64_t S_img, int B, int H, int D,
+                                   const int32_t *axes_dims, int n_axes, double theta, void *out,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace of flux_joint_rope_attention_rows with the exchange buffer; 0 for
+ * unsupported sizes. */
+size_t flux_joint_rope_attention_rows_workspace(int B, int64_t S_q, int64_t S, int H, int D);
 
 /*
  * flux_joint_rope_attention_tabled: the same attention, with the RoPE table
