@@ -56,7 +56,10 @@ const char *flux_status_string(int status) {
     case FLUX_ERR_DEVICE_TIMEOUT: return "a kernel gave up a bounded wait (device timeout)";
     case FLUX_ERR_UNSUPPORTED: return "the current device is not sm_103 (GB300)";
     case FLUX_ERR_ALIAS: return "an output or scratch buffer overlaps an input or another output";
-    default: return "unknown status";
+    default:
+      if (status < FLUX_DEBUG_STATUS_BASE && status > FLUX_DEBUG_STATUS_BASE - 100)
+        return "a checked index was out of range (checked build)";
+      return "unknown status";
   }
 }
 

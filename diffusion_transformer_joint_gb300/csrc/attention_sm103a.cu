@@ -373,13 +373,52 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Checked build (-DFLUX_DEBUG): before each shared-memory, TMEM, TMA and
+// global (exchange buffer, flags, tables, inputs, output) access site listed
+// in DbgSite, the kernel checks that the region, stage, lane quadrant, column
+// range, coordinates and row range it is about to use lie inside what that
+// site may touch. A failed check skips the access and records its site (the
+// first one of the launch); at exit the CTA writes FLUX_DEBUG_STATUS_BASE -
+// site into the status word. Nothing traps. Release builds compile every
+// check to `true`.
+enum DbgSite {
+  kDbgQLoad = 1,       // producer: Q tile copies (raw or rotated)
+  kDbgKLoad = 2,       // producer: K tile copies (raw, rotated or pre-rotated)
+  kDbgFlagRead = 3,    // producer: publication flags of a K tile
+  kDbgVLoad = 4,       // V producer: V tile copies
+  kDbgMmaS = 5,        // MMA: S = Q K^T operands
+  kDbgMmaPV = 6,       // MMA: O += P V operands
+  kDbgSLoad = 7,       // softmax: S columns read from TMEM
+  kDbgORescale = 8,    // softmax: O columns rescaled in TMEM
+  kDbgPStore = 9,      // softmax: P columns written to TMEM
+  kDbgOLoad = 10,      // epilogue: O columns read from TMEM
+  kDbgStage = 11,      // epilogue: per-warp staging buffer
+  kDbgOutRow = 12,     // epilogue: row-by-row global stores
+  kDbgOutTma = 13,     // epilogue: TMA tile stores
+  kDbgTableLoad = 14,  // RoPE: table rows copied to shared memory
+  kDbgQRotate = 15,    // RoPE: Q tile rotated in place
+  kDbgKRotate = 16,    // RoPE: K tile rotated in place and published
+  kDbgPrepare = 17,    // RoPE: next item's rows rotated global to global
+  kDbgQueue = 18,      // RoPE: work queue entry decoded
+};
+#ifdef FLUX_DEBUG
+__device__ int g_dbg_site;  // first failed check of the current launch, 0 if none
+__device__ __forceinline__ bool dbg_check(bool ok, int site) {
+  if (!ok) atomicCAS(&g_dbg_site, 0, site);
+  return ok;
+}
+#define FLUX_DBG(cond, site) dbg_check((cond), (site))
+#else
+#define FLUX_DBG(cond, site) true
+#endif
+
 // kNorm: Q and K are RMS-normalised (qn / kn) before the rotation.
 template <bool kNorm>
 __global__ void __launch_bounds__(kThreads, 1)
     joint_rope_attention_kernel(const __grid_constant__ Maps maps, uint16_t *__restrict__ outg,
                                 int *__restrict__ status,
-                                const Segs sg, int64_t S_q, int64_t S_k, int H, int h0, int Hl,
-                                int n_items,
+                                const Segs sg, int B, int64_t S_q, int64_t S_k, int H, int h0,
+                                int Hl, int n_items, int64_t n_flag_words,
                                 uint64_t *__restrict__ kflags, uint16_t *__restrict__ krot,
                                 uint16_t *__restrict__ qrot, const uint16_t *__restrict__ qg,
                                 const uint16_t *__restrict__ kg,
@@ -398,6 +437,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = static_cast<int>(threadIdx.x);
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // [addr, addr + bytes) inside the shared-memory region [off, off + size)
+  auto in_smem = [&](uint32_t addr, uint32_t bytes, uint32_t off, uint32_t size) {
+    return addr >= sbase + off && addr + bytes <= sbase + off + size;
+  };
+  (void)in_smem;
   // token strides (elements) of Q / K / V / out (all H heads) and of the
   // exchange buffer (the launch's Hl heads h0 .. h0 + Hl - 1)
   const int64_t row_stride = static_cast<int64_t>(H) * kD;
@@ -485,6 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem = *tmem_slot;
+  // TMEM columns [col, col + n) of this warp's lane quadrant, inside [lo, hi)
+  // of the allocation
+  auto in_tmem = [&](uint32_t taddr, uint32_t n, uint32_t lo, uint32_t hi) {
+    const uint32_t col = (taddr & 0xFFFFu) - (tmem & 0xFFFFu);
+    return (taddr >> 16) - (tmem >> 16) == static_cast<uint32_t>((warp & 3) * 32) && col >= lo &&
+           col + n <= hi && hi <= kTmemCols;
+  };
+  (void)in_tmem;
 
   const uint32_t idesc_qk = idesc_bf16_f32(128, 128, 0, 0);
   const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
@@ -539,18 +591,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           fence_proxy_async_global();
           last_q_bar = kBarQFull;
           last_q_parity = static_cast<uint32_t>(k) & 1u;
-          mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
-          for (int t = 0; t < kQTiles; ++t) {
-            const uint32_t dst = sbase + kOffQ + t * kTileBytes;
-            tma_load_4d(dst, &maps.qrot, bar(kBarQFull), 0, hx, m0 + t * kBM, b);
-            tma_load_4d(dst + kBlockBytes, &maps.qrot, bar(kBarQFull), 64, hx, m0 + t * kBM, b);
+          if (FLUX_DBG(hx < Hl && b < B && m0 >= 0 && m0 < S_q, kDbgQLoad)) {
+            mbar_arrive_expect_tx(bar(kBarQFull), kQTiles * kTileBytes);
+            for (int t = 0; t < kQTiles; ++t) {
+              const uint32_t dst = sbase + kOffQ + t * kTileBytes;
+              tma_load_4d(dst, &maps.qrot, bar(kBarQFull), 0, hx, m0 + t * kBM, b);
+              tma_load_4d(dst + kBlockBytes, &maps.qrot, bar(kBarQFull), 64, hx, m0 + t * kBM, b);
+            }
+          } else {
+            mbar_arrive(bar(kBarQFull));  // checked build: no copy, the phase still completes
           }
           mbar_arrive_n(bar(kBarQFull), 3);
         } else {
           last_q_bar = kBarQRaw;
           last_q_parity = static_cast<uint32_t>(q_local) & 1u;
-          mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
-          for (int t = 0; t < kQTiles; ++t) {
+          const bool q_ok = FLUX_DBG(h < H && b < B && m0 >= 0 && m0 < S_q, kDbgQLoad);
+          if (q_ok) mbar_arrive_expect_tx(bar(kBarQRaw), kQTiles * kTileBytes);
+          else mbar_arrive(bar(kBarQRaw));  // checked build: no copy, the phase still completes
+          for (int t = 0; q_ok && t < kQTiles; ++t) {
             const uint32_t dst = sbase + kOffQ + t * kTileBytes;
             tma_load_4d(dst, &maps.q, bar(kBarQRaw), 0, h, m0 + t * kBM, b);
             tma_load_4d(dst + kBlockBytes, &maps.q, bar(kBarQRaw), 64, h, m0 + t * kBM, b);
@@ -579,7 +637,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Pre-rotated tiles need no rotation at all.
           const bool pre = tj >= it.n_main;
           bool rotated = pre || (share && k > 0 && j < 2);
-          if (share && !rotated) {
+          if (share && !rotated &&
+              FLUX_DBG(it.flags - kflags + static_cast<int64_t>(tj) * 4 + 4 <= n_flag_words &&
+                           tj < it.n_main,
+                       kDbgFlagRead)) {
             const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
             ld_relaxed_gpu_v2_u64(fl, f0, f1);
@@ -591,7 +652,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
-          if (share && !rotated) {
+          if (share && !rotated &&
+              FLUX_DBG(it.flags - kflags + static_cast<int64_t>(tj) * 4 + 4 <= n_flag_words,
+                       kDbgFlagRead)) {
             // A second look once the ring slot is free: decided early, the
             // first look misses tiles the CTAs that started the head at the
             // same time publish while this one waits (the first item's tiles
@@ -607,7 +670,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const uint32_t dst = sbase + kOffK + s * kTileBytes;
-          if (rotated) {
+          if (!FLUX_DBG(in_smem(dst, kTileBytes, kOffK, kStages * kTileBytes) && tj >= 0 &&
+                            tj < it.n_tiles && krow >= 0 &&
+                            krow < (pre ? it.n_pre : it.k_hi) && krow >= (pre ? 0 : it.k_lo) &&
+                            h < H && hx < Hl && b < B,
+                        kDbgKLoad)) {
+            // checked build: no copy; K-full completes without it
+            last_k_full |= 1u << s;
+            last_k_par = (last_k_par & ~(1u << s)) | ((use & 1u) << s);
+            mbar_arrive_n(bar(kBarKFull + s), 4);
+          } else if (rotated) {
             // straight to the MMA: the copy completes K-full, whose other
             // three arrivals are made here
             last_k_full |= 1u << s;
@@ -670,6 +742,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           const uint32_t dst = sbase + kOffV + s * kTileBytes;
+          const bool main_tile = tj < it.n_main;
+          if (!FLUX_DBG(in_smem(dst, kTileBytes, kOffV, kStages * kTileBytes) && tj >= 0 &&
+                            tj < it.n_tiles && vrow >= (main_tile ? it.k_lo : 0) &&
+                            vrow < (main_tile ? it.k_hi : it.n_pre) && h < H && b < B,
+                        kDbgVLoad)) {
+            mbar_arrive(bar(kBarVFull + s));  // checked build: no copy, the phase completes
+            continue;
+          }
           mbar_arrive_expect_tx(bar(kBarVFull + s), kTileBytes);
           tma_load_4d(dst, src, bar(kBarVFull + s), 0, h, vrow, b);
           tma_load_4d(dst + kBlockBytes, src, bar(kBarVFull + s), 64, h, vrow, b);
@@ -697,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dk0 = desc_kmajor(sbase + kOffK, 0);
       const uint64_t dv0 = desc_v(sbase + kOffV, 0);
       auto issue_s = [&](int t, int sk) {
+        if (!FLUX_DBG(t >= 0 && t < kQTiles && sk >= 0 && sk < kStages, kDbgMmaS)) return;
         uint64_t da = desc_advance(dq0, t * kTileBytes);
         uint64_t db = desc_advance(dk0, sk * kTileBytes);
         opaque(da);  // per-MMA descriptors are base + constant, computed here,
@@ -745,10 +826,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       abort_flag)))
               break;
             tc_fence_after_sync();
+            if (FLUX_DBG(t >= 0 && t < kQTiles && sv >= 0 && sv < kStages, kDbgMmaPV)) {
 #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, desc_advance(dv, kk * 2048),
-                           idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                             desc_advance(dv, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+            }
             mma_commit_elect(bar(kBarODone + t));
             if (t == kQTiles - 1) mma_commit_elect(bar(kBarVEmpty + sv));
             if (more) {
@@ -795,6 +878,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         uint32_t sr[kBN];
         float mr[kBN / 32];
+        if (!FLUX_DBG(in_tmem(tS, kBN, t * 128, t * 128 + 128), kDbgSLoad)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c)
           tmem_ld32_max(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]), mr[c]);
@@ -827,6 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S_t(j) is complete, hence so is PV_t(j-1): O_t is stable here.
 #pragma unroll 1
           for (int c = 0; c < kD / 16; ++c) {
+            if (!FLUX_DBG(in_tmem(tO + c * 16, 16, 256 + t * 128, 384 + t * 128), kDbgORescale))
+              continue;
             uint32_t o[16];
             tmem_ld16(tO + c * 16, o);
             tmem_ld_wait();
@@ -855,7 +944,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[(i >> 1) & 3] = f2_add(acc[(i >> 1) & 3], f2_pack(p0, p1));
             pk[i / 2] = pack_bf16x2(p0, p1);
           }
-          tmem_st16(tS + c * 16, pk);
+          if (FLUX_DBG(in_tmem(tS + c * 16, 16, t * 128, t * 128 + 64), kDbgPStore))
+            tmem_st16(tS + c * 16, pk);
         }
         float sum;
         {
@@ -887,6 +977,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < kD / 32; ++c) {
         uint32_t o[32];
+        if (!FLUX_DBG(in_tmem(tO + c * 32, 32, 256 + t * 128, 384 + t * 128) &&
+                          in_smem(stage, kStageWarpBytes, kOffStage, 8 * kStageWarpBytes),
+                      kDbgOLoad))
+          continue;
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait();
         if (lane == 0) bulk_wait_read_all();  // the previous copy has read the buffer
@@ -899,16 +993,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           w.y = pack_bf16x2(__uint_as_float(o[8 * q + 2]) * inv_l, __uint_as_float(o[8 * q + 3]) * inv_l);
           w.z = pack_bf16x2(__uint_as_float(o[8 * q + 4]) * inv_l, __uint_as_float(o[8 * q + 5]) * inv_l);
           w.w = pack_bf16x2(__uint_as_float(o[8 * q + 6]) * inv_l, __uint_as_float(o[8 * q + 7]) * inv_l);
-          if (box_ok)
-            st_shared_v4(stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4), w);
-          else if (row_ok)
+          const uint32_t sa = stage + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+          if (box_ok) {
+            if (FLUX_DBG(in_smem(sa, 16, kOffStage + (warp - 4) * kStageWarpBytes,
+                                 kStageWarpBytes),
+                         kDbgStage))
+              st_shared_v4(sa, w);
+          } else if (row_ok &&
+                     FLUX_DBG(b < B && h < H && row0 + lane >= 0 && row0 + lane < S_q,
+                              kDbgOutRow)) {
             st_global_v4(outg + ((static_cast<int64_t>(b) * S_q + row0 + lane) * H + h) * kD +
                              c * 32 + q * 8,
                          w);
+          }
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && box_ok) {
+        if (lane == 0 && box_ok &&
+            FLUX_DBG(row0 >= 0 && row0 < S_q && c * 32 < kD && h < H && b < B, kDbgOutTma)) {
           tma_store_4d(&maps.out, stage, c * 32, h, static_cast<int>(row0), b);
           bulk_commit();
         }
@@ -936,8 +1038,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   abort_flag)))
           return;
         if (lane == 0) {
-          mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
-          tma_load_2d(sbase + kOffT, tmap, bar(kBarTFull), 0, static_cast<int>(row0));
+          const int64_t rows = tmap == &maps.table_q ? S_q : S_k;
+          if (FLUX_DBG(row0 >= 0 && row0 < rows && (tmap == &maps.table_q || tmap == &maps.table_k),
+                       kDbgTableLoad)) {
+            mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
+            tma_load_2d(sbase + kOffT, tmap, bar(kBarTFull), 0, static_cast<int>(row0));
+          } else {
+            mbar_arrive(bar(kBarTFull));  // checked build: no copy, the phase completes
+          }
         }
         __syncwarp();
         ++tload;
@@ -994,11 +1102,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tab = tabk;
         }
         const int nrows = static_cast<int>(n_rows - tok0 < 64 ? (n_rows - tok0 > 0 ? n_rows - tok0 : 0) : 64);
-        if (nrows > 0)
+        // rows tok0 .. tok0 + nrows - 1 of head h (inputs) / hx (exchange buffer) of batch b
+        const bool prep_ok = FLUX_DBG(
+            tok0 >= 0 && tok0 + nrows <= n_rows && nx.b < B && nx.h < H && nx.hx < Hl &&
+                (c < 4 || nx.flags - kflags + static_cast<int64_t>(tile_at(nx, kt)) * 4 + 4 <=
+                              n_flag_words),
+            kDbgPrepare);
+        if (nrows > 0 && prep_ok)
           rotate_rows_global<kNorm>(src, dst, tab + tok0 * kPairs, nrows, row_stride, xrow_stride,
                                     u, c < 4 ? qn : kn, tok0);
         fence_proxy_async_global();  // read by TMA copies
-        if (c >= 4 && ((c - 4) & 1) == 1) {
+        if (c >= 4 && ((c - 4) & 1) == 1 && prep_ok) {
           // publish as the in-place path does: this warp's rows, then its flag
           fence_acq_rel_gpu();
           __syncwarp();
@@ -1027,6 +1141,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t kind = x & 15u;
       if (kind == kRqEnd) break;
       const int item = static_cast<int>(y);
+      if (!FLUX_DBG(kind >= kRqQ && kind <= kRqPrep && item >= 0 && item < n_items &&
+                        (kind != kRqPrep || ((x >> 4) & 15u) < static_cast<uint32_t>(kPrepChunks)) &&
+                        (kind != kRqK || (((x >> 4) & 15u) < static_cast<uint32_t>(kStages) &&
+                                          static_cast<int>(x >> 9) < info(item).n_tiles)),
+                    kDbgQueue)) {
+        ok = false;
+        break;
+      }
       if (kind == kRqPrep) {
         prepare_piece(item, static_cast<int>((x >> 4) & 15u));
         continue;
@@ -1039,6 +1161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
         for (int t = 0; ok && t < kQTiles; ++t) {
           if (t > 0) load_table(&maps.table_q, it.m0 + t * kBM);
+          FLUX_DBG(it.m0 >= 0 && it.m0 < S_q, kDbgQRotate);  // rotation stays in smem
           rotate_tile(sbase + kOffQ + t * kTileBytes, it.m0 + t * kBM, S_q, nullptr, qn,
                       &maps.table_q);
         }
@@ -1054,12 +1177,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       load_table(&maps.table_k, tok0);  // in flight while the tile itself lands
       if (!ok) break;
       if (!(ok = mbar_wait_warp(bar(kBarKRaw + s), par, abort_flag))) break;
-      uint16_t *grow =
-          share ? krot + ((static_cast<int64_t>(it.b) * S_k + tok0) * Hl + it.hx) * kD : nullptr;
+      // publication: rows tok0 .. of head hx in the exchange buffer and this
+      // warp's flag of tile tj
+      const bool pub_ok = FLUX_DBG(
+          tok0 >= 0 && tok0 < S_k && it.b < B && it.hx < Hl && s < kStages &&
+              (!share || it.flags - kflags + static_cast<int64_t>(tj) * 4 + 4 <= n_flag_words),
+          kDbgKRotate);
+      uint16_t *grow = share && pub_ok
+                           ? krot + ((static_cast<int64_t>(it.b) * S_k + tok0) * Hl + it.hx) * kD
+                           : nullptr;
       rotate_tile(sbase + kOffK + s * kTileBytes, tok0, S_k, grow, kn, &maps.table_k);
       if (!ok) break;
       fence_proxy_async_smem();
-      if (share) {
+      if (share && pub_ok) {
         // publish this warp's rows of tile tj: each lane's stores, then
         // one flag per warp (release)
         fence_proxy_async_global();
@@ -1086,6 +1216,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     grid_dep_wait();  // after the table kernel's clear of the same word
     atomicExch(status, FLUX_ERR_DEVICE_TIMEOUT);
   }
+#ifdef FLUX_DEBUG
+  if (tid == 0) {  // a failed check outranks the timeout it may have caused
+    const int site = atomicAdd(&g_dbg_site, 0);
+    if (site != 0) {
+      grid_dep_wait();
+      atomicExch(status, FLUX_DEBUG_STATUS_BASE - site);
+    }
+  }
+#endif
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
@@ -1273,6 +1412,15 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
   const unsigned grid = static_cast<unsigned>(items < sms ? items : sms);
   const uint16_t *qg = static_cast<const uint16_t *>(q), *kg = static_cast<const uint16_t *>(k);
   uint16_t *og = static_cast<uint16_t *>(out);
+#ifdef FLUX_DEBUG
+  {  // checked build: clear the first-failure record; no overlap with the table kernel
+    void *site = nullptr;
+    e = cudaGetSymbolAddress(&site, g_dbg_site);
+    if (e == cudaSuccess) e = cudaMemsetAsync(site, 0, sizeof(int), stream);
+    if (e != cudaSuccess) return e;
+    pdl = false;
+  }
+#endif
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -1284,18 +1432,19 @@ cudaError_t launch_attention_segments(const void *q, const void *k, const void *
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   const int n_items = static_cast<int>(items);
+  const int64_t n_flag_words = xbuf != nullptr ? off : 0;
   const uint64_t token = next_launch_token();
   if (norm != nullptr) {
     const QkNorm qn{norm->q_txt, norm->q_img, norm->s_txt, norm->eps};
     const QkNorm kn{norm->k_txt, norm->k_img, norm->s_txt, norm->eps};
-    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<true>, maps, og, status, sg, S_q, S_k,
-                           H, h0, Hl, n_items, kflags, krot, qrot, qg, kg, table_q, table_k, token,
-                           qn, kn);
+    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<true>, maps, og, status, sg, B, S_q,
+                           S_k, H, h0, Hl, n_items, n_flag_words, kflags, krot, qrot, qg, kg,
+                           table_q, table_k, token, qn, kn);
   } else {
     const QkNorm none{nullptr, nullptr, 0, 0.f};
-    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<false>, maps, og, status, sg, S_q,
-                           S_k, H, h0, Hl, n_items, kflags, krot, qrot, qg, kg, table_q, table_k,
-                           token, none, none);
+    e = cudaLaunchKernelEx(&cfg, joint_rope_attention_kernel<false>, maps, og, status, sg, B,
+                           S_q, S_k, H, h0, Hl, n_items, n_flag_words, kflags, krot, qrot, qg, kg,
+                           table_q, table_k, token, none, none);
   }
   return e != cudaSuccess ? e : cudaGetLastError();
 }

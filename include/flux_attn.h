@@ -68,6 +68,13 @@ typedef enum {
   FLUX_ERR_ALIAS = -9           /* an output or scratch buffer overlaps an input or another output */
 } flux_status;
 
+/* Checked builds of the library only (compiled with -DFLUX_DEBUG): when one of
+ * the attention kernel's index checks fails, the kernel skips that access and
+ * its status word reads FLUX_DEBUG_STATUS_BASE - site, site >= 1 naming the
+ * access (see DbgSite in csrc/attention_sm103a.cu). Release builds never
+ * produce these codes. */
+#define FLUX_DEBUG_STATUS_BASE (-1000)
+
 /* Largest number of RoPE axes accepted (FLUX.2 uses 4). */
 #define FLUX_MAX_AXES 8
 
