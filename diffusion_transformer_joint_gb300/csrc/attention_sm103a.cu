@@ -1038,8 +1038,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                   abort_flag)))
           return;
         if (lane == 0) {
+          // a tile's table rows start inside the sequence or, for the later
+          // quarters of a ragged last 256-row block, up to 192 rows past its
+          // end (the copy then reads zeros, as the tile itself does)
           const int64_t rows = tmap == &maps.table_q ? S_q : S_k;
-          if (FLUX_DBG(row0 >= 0 && row0 < rows && (tmap == &maps.table_q || tmap == &maps.table_k),
+          if (FLUX_DBG(row0 >= 0 && row0 < rows + 192 && (row0 & 63) == 0 &&
+                           (tmap == &maps.table_q || tmap == &maps.table_k),
                        kDbgTableLoad)) {
             mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
             tma_load_2d(sbase + kOffT, tmap, bar(kBarTFull), 0, static_cast<int>(row0));
@@ -1104,7 +1108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int nrows = static_cast<int>(n_rows - tok0 < 64 ? (n_rows - tok0 > 0 ? n_rows - tok0 : 0) : 64);
         // rows tok0 .. tok0 + nrows - 1 of head h (inputs) / hx (exchange buffer) of batch b
         const bool prep_ok = FLUX_DBG(
-            tok0 >= 0 && tok0 + nrows <= n_rows && nx.b < B && nx.h < H && nx.hx < Hl &&
+            tok0 >= 0 && (nrows == 0 || tok0 + nrows <= n_rows) && nx.b < B && nx.h < H &&
+                nx.hx < Hl &&
                 (c < 4 || nx.flags - kflags + static_cast<int64_t>(tile_at(nx, kt)) * 4 + 4 <=
                               n_flag_words),
             kDbgPrepare);
