@@ -742,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           if (!(ok = mbar_wait(bar(kBarVEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           const uint32_t dst = sbase + kOffV + s * kTileBytes;
-          const bool main_tile = tj < it.n_main;
+          [[maybe_unused]] const bool main_tile = tj < it.n_main;
           if (!FLUX_DBG(in_smem(dst, kTileBytes, kOffV, kStages * kTileBytes) && tj >= 0 &&
                             tj < it.n_tiles && vrow >= (main_tile ? it.k_lo : 0) &&
                             vrow < (main_tile ? it.k_hi : it.n_pre) && h < H && b < B,
@@ -862,7 +862,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     reg_inc<kRegsSoftmax>();
     const int t = (warp - 4) >> 2;  // Q tile
     const int wq = warp & 3;        // TMEM lane quadrant
-    const int row = wq * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t tS = tmem + t * 128 + lane_off;
     const uint32_t tO = tmem + 256 + t * 128 + lane_off;
@@ -1039,10 +1038,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           return;
         if (lane == 0) {
           // a tile's table rows start inside the sequence or, for the later
-          // quarters of a ragged last 256-row block, up to 192 rows past its
-          // end (the copy then reads zeros, as the tile itself does)
-          const int64_t rows = tmap == &maps.table_q ? S_q : S_k;
-          if (FLUX_DBG(row0 >= 0 && row0 < rows + 192 && (row0 & 63) == 0 &&
+          // 64-row pieces of a ragged last 256-row block, up to 192 rows past
+          // its end (the copy then reads zeros, as the tile itself does);
+          // segment boundaries put the start anywhere
+          [[maybe_unused]] const int64_t rows = tmap == &maps.table_q ? S_q : S_k;
+          if (FLUX_DBG(row0 >= 0 && row0 < rows + 192 &&
                            (tmap == &maps.table_q || tmap == &maps.table_k),
                        kDbgTableLoad)) {
             mbar_arrive_expect_tx(bar(kBarTFull), kTableBytes);
@@ -1166,7 +1166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(bar(kBarQRaw), par, abort_flag))) break;
         for (int t = 0; ok && t < kQTiles; ++t) {
           if (t > 0) load_table(&maps.table_q, it.m0 + t * kBM);
-          FLUX_DBG(it.m0 >= 0 && it.m0 < S_q, kDbgQRotate);  // rotation stays in smem
+          (void)FLUX_DBG(it.m0 >= 0 && it.m0 < S_q, kDbgQRotate);  // rotation stays in smem
           rotate_tile(sbase + kOffQ + t * kTileBytes, it.m0 + t * kBM, S_q, nullptr, qn,
                       &maps.table_q);
         }
