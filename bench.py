@@ -241,7 +241,7 @@ def run_ours(args, rank, world, local_rank):
     t_max = max_over_ranks(total_ms, dist, dev)
 
     # end-to-end through the public one-call API with host buffers
-    e2e = run_e2e(w, dev, K, args.warmup, binding, W, torch, np, txt_np, img_np)
+    e2e = run_e2e(w, dev, K, args.warmup, binding, W, torch, np, txt_np, img_np, qk_norm)
     e2e["ms_per_step"] = max_over_ranks(e2e["ms_per_step"], dist, dev)
 
     if rank != 0:
@@ -304,7 +304,8 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": round(whole_job_tflops(flops_step, world, 1, e2e["ms_per_step"]), 2),
                 "unit": UNIT, "ms_per_step": round(e2e["ms_per_step"], 4),
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-                "api": "flux_joint_rope_attention (one call: tables + attention)",
+                "api": ("flux_joint_qknorm_rope_attention" if args.qk_norm else
+                        "flux_joint_rope_attention") + " (one call: tables + attention)",
                 "pipelining": PIPELINING},
         "gpu_launches": 2 * K,
     }
@@ -363,7 +364,7 @@ def two_lane_ms(torch, dev, K, warmup, lanes, one):
     return e0.elapsed_time(e1) / K
 
 
-def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
+def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np, qk_norm=None):
     """Same metric through the one-call API: every step copies its inputs from
     pinned host memory, runs the call and copies the output back. Steps
     alternate between two streams with their own device buffers and
@@ -393,7 +394,7 @@ def run_e2e(w, dev, K, warmup, binding, W, torch, np, txt_np, img_np):
                 d.copy_(h, non_blocking=True)
             dq, dk, dv, dtxt, dimg = ln["in"]
             binding.joint_rope_attention(dq, dk, dv, dtxt, dimg, out=ln["out"],
-                                         workspace=ln["ws"], stream=st)
+                                         workspace=ln["ws"], stream=st, qk_norm=qk_norm)
             ln["hout"].copy_(ln["out"], non_blocking=True)
 
     ms = two_lane_ms(torch, dev, K, warmup, lanes, one)
