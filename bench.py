@@ -58,8 +58,14 @@ def _peaks():
 
 
 def _kernel_hash(source=KERNEL_SOURCE):
-    with open(source, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of a kernel source's code: // comments, trailing blanks and blank
+    lines are left out, so that a comment edit does not orphan a profile."""
+    import re
+
+    with open(source, encoding="utf-8") as f:
+        lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in f]
+    code = "\n".join(ln for ln in lines if ln)
+    return hashlib.sha256(code.encode("utf-8")).hexdigest()[:16]
 
 
 def _profiled_traffic(summary=PROFILE_SUMMARY, source=KERNEL_SOURCE,

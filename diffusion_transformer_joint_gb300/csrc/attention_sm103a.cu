@@ -277,9 +277,9 @@ __device__ __forceinline__ void rotate_half(uint32_t tile, uint32_t tbl, int hal
 // 128 RoPE threads rotate `nrows` rows of one head from global memory to
 // global memory: src / dst point at the first row's channel 0, rows are
 // src_stride / dst_stride elements apart, `tab` at the first row's packed
-// table row. Thread
-// u owns 16-byte chunk u & 15 of rows (u >> 4) + 8 i, the row-to-thread map of
-// rotate_half, so RoPE warp w writes the rows r with r mod 8 in {2w, 2w+1}.
+// table row. Thread u owns 16-byte chunk u & 15 of rows (u >> 4) + 8 i, the
+// row-to-thread map of rotate_half, so RoPE warp w writes the rows r with
+// r mod 8 in {2w, 2w+1}.
 // With kNorm the rows (token tok0 + r) are RMS-normalised first; every lane
 // of the warp runs every iteration (rows past nrows are zeros, not stored).
 template <bool kNorm>
@@ -320,8 +320,8 @@ struct Maps {
 
 // A work item: batch b, head h of Q / K / V / out (hx: its index among the
 // launch's heads, which lay out the exchange buffer), the 256 query rows from
-// m0 (rows of Q / out
-// at or past q_hi belong to another segment: computed, never stored), its key
+// m0 (rows of Q / out at or past q_hi belong to another segment: computed,
+// never stored), its key
 // range: rows [k_lo, k_hi) of K / V in n_main 128-key tiles, then rows
 // [0, n_pre) of the pre-rotated K / V in the remaining tiles of n_tiles, all
 // walked from tile j0; and the publication flags of the n_main tiles for
