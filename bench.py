@@ -330,7 +330,12 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 2 * K,
     }
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, target_s=args.cpu_seconds)
+        gpu_out = sets[0][3].float().cpu().numpy()  # the last output of the first input set
+        norm_np = None
+        if qk_norm is not None:
+            norm_np = tuple(x.cpu().numpy() for x in qk_norm[:4]) + (qk_norm[4],)
+        line["cpu_baseline"], line["parity"] = cpu_baseline(
+            w, target_s=args.cpu_seconds, gpu_out=gpu_out, qk_norm=norm_np)
     return line
 
 
@@ -801,11 +806,14 @@ def run_proj(args, rank, world, local_rank):
 # --------------------------------------------------------- CPU baseline
 
 
-def _oracle_sample(w, rows, threads, q, k, v, txt, img):
+def _oracle_sample(w, rows, threads, q, k, v, txt, img, qk_norm=None, result=None):
     import oracle
 
     t0 = time.perf_counter()
-    oracle.joint_rope_attention(q, k, v, txt, img, rows=rows, threads=threads)
+    out = oracle.joint_rope_attention(q, k, v, txt, img, rows=rows, threads=threads,
+                                      qk_norm=qk_norm)
+    if result is not None:
+        result.append(out)
     return time.perf_counter() - t0
 
 
@@ -828,20 +836,34 @@ def _rows_for(w, seconds, threads, inputs):
     return np.linspace(0, w.S - 1, n).astype(np.int64)
 
 
-def cpu_baseline(w, target_s=12.0):
+def cpu_baseline(w, target_s=12.0, gpu_out=None, qk_norm=None):
     """The oracle as it stands, timed on the host cores on a bounded sample of
-    query rows (all batch elements and heads of each row) of the workload."""
+    query rows (all batch elements and heads of each row) of the workload.
+    With ``gpu_out`` (the GPU's output for the same inputs, as a float array)
+    the oracle's rows also check it: (baseline, parity) is returned."""
+    import numpy as np
+
     import oracle
 
     threads = oracle.default_threads()
     inputs = _oracle_inputs(w)
     rows = _rows_for(w, target_s, threads, inputs)
-    t = _oracle_sample(w, rows, threads, *inputs)
+    ref = []
+    t = _oracle_sample(w, rows, threads, *inputs, qk_norm=qk_norm, result=ref)
     flops = 4 * w.B * w.H * rows.size * w.S * w.D
-    return {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": threads,
+    base = {"value": round(flops / t / 1e12, 6), "unit": UNIT, "cores": threads,
             "kind": "oracle",
             "sample": f"{rows.size} of {w.S} query rows x all {w.B * w.H} (batch, head) pairs of "
                       f"{w.name} against all {w.S} keys, fp64, {t:.1f} s"}
+    if gpu_out is None:
+        return base
+    err = np.abs(np.asarray(gpu_out, dtype=np.float64)[:, rows] - ref[0])
+    parity = {"rows": int(rows.size), "elements": int(err.size),
+              "max_abs": float(err.max()), "mean_abs": float(err.mean()),
+              "bar": "max <= 1e-2, mean <= 1e-3",
+              "pass": bool(err.max() <= 1e-2 and err.mean() <= 1e-3),
+              "against": "fp64 oracle rows of the first input set, the timed steps' output"}
+    return base, parity
 
 
 def _percentiles(xs, ps):

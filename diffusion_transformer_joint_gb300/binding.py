@@ -46,7 +46,14 @@ _lib = None
 
 
 def library_path() -> str:
-    return os.environ.get("FLUX_ATTN_LIB", _build.LIB_PATH)
+    """FLUX_ATTN_LIB if set; else the checked build when FLUX_ATTN_DEBUG=1
+    (build it with ``python -m diffusion_transformer_joint_gb300.build
+    --checked``); else the release build."""
+    if "FLUX_ATTN_LIB" in os.environ:
+        return os.environ["FLUX_ATTN_LIB"]
+    if os.environ.get("FLUX_ATTN_DEBUG") == "1":
+        return _build.CHECKED_LIB_PATH
+    return _build.LIB_PATH
 
 
 def load(path: str | None = None):

@@ -1,6 +1,10 @@
 """Builds the CUDA library libflux_attn.so in-tree with nvcc for sm_103a.
 
-Usage: ``python -m diffusion_transformer_joint_gb300.build [--force]``.
+Usage: ``python -m diffusion_transformer_joint_gb300.build [--force] [--checked]``.
+``--checked`` builds libflux_attn_checked.so instead: the same library compiled
+with -DFLUX_DEBUG, whose attention kernel checks its shared-memory, TMEM, TMA
+and exchange-buffer accesses and reports a failed check in the status word
+(the binding loads it when FLUX_ATTN_DEBUG=1).
 """
 from __future__ import annotations
 
@@ -16,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libflux_attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+CHECKED_LIB_PATH = os.path.join(BUILD_DIR, "libflux_attn_checked.so")
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -44,7 +49,7 @@ def build(force: bool = False, out: str = LIB_PATH, defines=(), verbose: bool = 
     os.makedirs(os.path.dirname(out), exist_ok=True)
     if not force and os.path.exists(out):
         t = os.path.getmtime(out)
-        if all(os.path.getmtime(p) <= t for p in _inputs()) and not defines:
+        if all(os.path.getmtime(p) <= t for p in _inputs()):
             return out
     tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC,
@@ -62,5 +67,13 @@ def build(force: bool = False, out: str = LIB_PATH, defines=(), verbose: bool = 
     return out
 
 
+def build_checked(force: bool = False, out: str = CHECKED_LIB_PATH) -> str:
+    """The checked library (-DFLUX_DEBUG) at ``out``; returns its path."""
+    return build(force=force, out=out, defines=("FLUX_DEBUG",))
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--checked" in sys.argv:
+        print(build_checked(force="--force" in sys.argv))
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))

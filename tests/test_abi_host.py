@@ -291,3 +291,21 @@ def test_norm_weight_shapes_checked_in_the_binding():
     # right shapes pass that check and stop at the device check (no CPU path)
     with pytest.raises(ValueError, match="CUDA"):
         binding._norm_args((good, good, good, good, 1e-6), "cpu")
+
+
+def test_checked_build_compiles_and_is_selected_by_the_environment(monkeypatch):
+    """The -DFLUX_DEBUG library builds (nvcc cross-compiles here), exports every
+    declared symbol, and is the one the binding picks with FLUX_ATTN_DEBUG=1."""
+    path = build.build_checked()
+    checked = ctypes.CDLL(path)
+    for name in _declared_symbols():
+        assert hasattr(checked, name), name
+    # a failed check's code reads as such; release codes are unchanged
+    checked.flux_status_string.restype = ctypes.c_char_p
+    assert b"checked" in checked.flux_status_string(-1005)
+    assert checked.flux_status_string(-7) == b"a kernel gave up a bounded wait (device timeout)"
+    monkeypatch.delenv("FLUX_ATTN_LIB", raising=False)
+    monkeypatch.setenv("FLUX_ATTN_DEBUG", "1")
+    assert binding.library_path() == build.CHECKED_LIB_PATH
+    monkeypatch.setenv("FLUX_ATTN_DEBUG", "0")
+    assert binding.library_path() == build.LIB_PATH

@@ -27,11 +27,9 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module")
-def libs(tmp_path_factory):
+def libs():
     release = binding.load(build.build())
-    out = tmp_path_factory.mktemp("checked") / "libflux_attn_checked.so"
-    build.build(force=True, out=str(out), defines=("FLUX_DEBUG",))
-    checked = ctypes.CDLL(str(out))
+    checked = ctypes.CDLL(build.build_checked())
     for name in binding.EXPORTS + ("flux_status_string",):
         fn_r, fn_c = getattr(release, name), getattr(checked, name)
         fn_c.argtypes, fn_c.restype = fn_r.argtypes, fn_r.restype
