@@ -643,13 +643,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                        kDbgFlagRead)) {
             const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
-            ld_relaxed_gpu_v2_u64(fl, f0, f1);
-            ld_relaxed_gpu_v2_u64(fl + 2, f2, f3);
+            // acquire loads: a set flag orders the publisher's rows before
+            // this thread's later accesses (a full GPU-scope fence here cost
+            // the producer more than the loads themselves)
+            ld_acquire_gpu_v2_u64(fl, f0, f1);
+            ld_acquire_gpu_v2_u64(fl + 2, f2, f3);
             rotated = f0 == token && f1 == token && f2 == token && f3 == token;
-            if (rotated) {
-              fence_acq_rel_gpu();         // acquire: the publishers' stores are visible
-              fence_proxy_async_global();  // to the TMA copy below as well
-            }
+            if (rotated) fence_proxy_async_global();  // ... and before the TMA copy below
           }
           if (!(ok = mbar_wait(bar(kBarKEmpty + s), (use & 1u) ^ 1u, abort_flag))) break;
           if (share && !rotated &&
@@ -661,13 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // after its own two).
             const uint64_t *fl = it.flags + static_cast<int64_t>(tj) * 4;
             uint64_t f0, f1, f2, f3;
-            ld_relaxed_gpu_v2_u64(fl, f0, f1);
-            ld_relaxed_gpu_v2_u64(fl + 2, f2, f3);
+            ld_acquire_gpu_v2_u64(fl, f0, f1);
+            ld_acquire_gpu_v2_u64(fl + 2, f2, f3);
             rotated = f0 == token && f1 == token && f2 == token && f3 == token;
-            if (rotated) {
-              fence_acq_rel_gpu();
-              fence_proxy_async_global();
-            }
+            if (rotated) fence_proxy_async_global();
           }
           const uint32_t dst = sbase + kOffK + s * kTileBytes;
           if (!FLUX_DBG(in_smem(dst, kTileBytes, kOffK, kStages * kTileBytes) && tj >= 0 &&

@@ -385,16 +385,17 @@ __device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) 
 
 // ------------------------------------------- cross-CTA hand-off in global
 
-// Two adjacent flag words (16-byte aligned), each read with relaxed strength.
-__device__ __forceinline__ void ld_relaxed_gpu_v2_u64(const uint64_t *p, uint64_t &a, uint64_t &b) {
-  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+// Two adjacent flag words (16-byte aligned) loaded with acquire semantics at
+// GPU scope: this thread's later accesses (after a proxy fence, its TMA copies
+// too) observe everything the flags' writers released before setting them.
+__device__ __forceinline__ void ld_acquire_gpu_v2_u64(const uint64_t *p, uint64_t &a, uint64_t &b) {
+  asm volatile("ld.acquire.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 // A flag word stored with relaxed strength at GPU scope.
 __device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t *p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-// With a relaxed flag store after it: a release; after a relaxed flag load
-// that saw the value: an acquire.
+// With a relaxed flag store after it: a release.
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
