@@ -525,9 +525,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
+  // The first item is prepared here by all 512 threads, before any role has
+  // work: its Q rows and its first two K tiles (those in the main key range)
+  // rotated into the exchange buffer, as the RoPE warps prepare every later
+  // item while the one before it runs. Thread t owns 16-byte chunk t & 15 of
+  // rows (t >> 4) + 32 i: i < 8 the item's 256 Q rows, i >= 8 rows of K tile
+  // (i - 8) >> 2. With the norm every thread runs every row (the row sums are
+  // shuffles across 16 lanes); rows past the tensor's end are not stored.
+  const bool first_prep = share && static_cast<int>(blockIdx.x) < n_items;
+  if (first_prep) {
+    grid_dep_wait();  // the rotation reads the tables
+    const Item it = info(static_cast<int>(blockIdx.x));
+    const bool prep_ok = FLUX_DBG(
+        it.b < B && it.h < H && it.hx < Hl && it.m0 >= 0 && it.m0 < S_q &&
+            it.flags - kflags + static_cast<int64_t>(it.n_main) * 4 <= n_flag_words,
+        kDbgPrepare);
+    const int r0 = tid >> 4, c16 = tid & 15;
+    constexpr int kB = kNorm ? 4 : 8;  // rows with loads in flight together
+#pragma unroll 1
+    for (int g = 0; g < 16; g += kB) {
+      const bool is_q = g < 8;
+      const NormW nw = kNorm ? load_norm_w(is_q ? qn : kn, c16) : NormW{};
+      uint4 w[kB], cs[kB];
+      int64_t tok[kB];
+      uint16_t *dst[kB];
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        bool valid;
+        const uint16_t *src;
+        const uint32_t *tab;
+        if (is_q) {
+          tok[i] = it.m0 + r0 + 32 * (g + i);
+          valid = tok[i] < S_q;
+          src = qg + ((static_cast<int64_t>(it.b) * S_q + tok[i]) * H + it.h) * kD;
+          dst[i] = qrot + ((static_cast<int64_t>(it.b) * S_q + tok[i]) * Hl + it.hx) * kD;
+          tab = tabq;
+        } else {
+          const int kt = (g + i - 8) >> 2;
+          const bool in_main = kt < it.n_tiles && tile_at(it, kt) < it.n_main;
+          tok[i] = (in_main ? tile_row(it, tile_at(it, kt)) : 0) + r0 + 32 * ((g + i - 8) & 3);
+          valid = in_main && tok[i] < S_k;
+          src = kg + ((static_cast<int64_t>(it.b) * S_k + tok[i]) * H + it.h) * kD;
+          dst[i] = krot + ((static_cast<int64_t>(it.b) * S_k + tok[i]) * Hl + it.hx) * kD;
+          tab = tabk;
+        }
+        if (!(valid && prep_ok)) dst[i] = nullptr;
+        w[i] = make_uint4(0u, 0u, 0u, 0u);
+        cs[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (dst[i] != nullptr) {
+          w[i] = ld_global_nc_v4(src + c16 * 8);
+          cs[i] = ld_global_nc_v4(tab + tok[i] * kPairs + c16 * 4);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kB; ++i) {
+        const uint4 o = rope_chunk<kNorm>(w[i], cs[i], is_q ? qn : kn, tok[i], nw);
+        if (dst[i] != nullptr) st_global_v4(dst[i] + c16 * 8, o);
+      }
+    }
+    fence_proxy_async_global();  // read by the producer's TMA copies
+    fence_acq_rel_gpu();         // ... and by other CTAs once the flags below are set
+  }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
+  if (first_prep && tid < 8) {
+    // publish the two K tiles: every thread's rows are written (the barrier
+    // above); one thread per flag word
+    const Item it = info(static_cast<int>(blockIdx.x));
+    const int kt = tid >> 2;
+    if (kt < it.n_tiles && tile_at(it, kt) < it.n_main &&
+        FLUX_DBG(it.flags - kflags + static_cast<int64_t>(tile_at(it, kt)) * 4 + 4 <= n_flag_words,
+                 kDbgPrepare)) {
+      fence_acq_rel_gpu();
+      st_relaxed_gpu_u64(it.flags + static_cast<int64_t>(tile_at(it, kt)) * 4 + (tid & 3), token);
+    }
+  }
   const uint32_t tmem = *tmem_slot;
   // TMEM columns [col, col + n) of this warp's lane quadrant, inside [lo, hi)
   // of the allocation
@@ -582,11 +655,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the previous item's S MMAs no longer read the Q buffers
         if (k > 0 && !(ok = mbar_wait(bar(kBarQFree), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
           break;
-        if (share && k > 0) {
-          // The RoPE warps rotated this item's Q into the exchange buffer
-          // during the previous item: copy it in rotated, completing Q-full
-          // (its other three arrivals made here) without the RoPE warps.
-          if (!(ok = mbar_wait(bar(kBarQPrep), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
+        if (share) {
+          // This item's Q is in the exchange buffer, rotated (the first
+          // item's by the whole CTA before the roles started, every later
+          // one's by the RoPE warps during the previous item): copy it in,
+          // completing Q-full (its other three arrivals made here) without
+          // the RoPE warps.
+          if (k > 0 &&
+              !(ok = mbar_wait(bar(kBarQPrep), static_cast<uint32_t>(k - 1) & 1u, abort_flag)))
             break;
           fence_proxy_async_global();
           last_q_bar = kBarQFull;
@@ -632,11 +708,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t use = static_cast<uint32_t>(jt / kStages);
           // Has every RoPE warp of some CTA published tile tj? Decided (and
           // the acquire fence paid) before the ring wait, which hides both.
-          // The first two tiles of a prepared item were rotated by this CTA's
-          // RoPE warps, ordered before this point by the Q-prep wait.
-          // Pre-rotated tiles need no rotation at all.
+          // The first two tiles of an item were rotated by this CTA, ordered
+          // before this point by the Q-prep wait (the first item's by the
+          // barrier before the roles). Pre-rotated tiles need no rotation.
           const bool pre = tj >= it.n_main;
-          bool rotated = pre || (share && k > 0 && j < 2);
+          bool rotated = pre || (share && j < 2);
           if (share && !rotated &&
               FLUX_DBG(it.flags - kflags + static_cast<int64_t>(tj) * 4 + 4 <= n_flag_words &&
                            tj < it.n_main,
