@@ -889,7 +889,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait_warp(bar(kBarVFull + sv), static_cast<uint32_t>(g0 / kStages) & 1u,
                                     abort_flag)))
             break;
-#pragma unroll 1
+          // unrolled: the issuer's own instructions are on the pipe's critical
+          // path (its loop overhead cost ~2% when this loop was kept rolled)
+#pragma unroll
           for (int t = 0; t < kQTiles; ++t) {
             if (!(ok = mbar_wait_warp(bar(kBarPFull + t), static_cast<uint32_t>(g0) & 1u, abort_flag)))
               break;
