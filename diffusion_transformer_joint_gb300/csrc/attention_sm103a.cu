@@ -227,7 +227,7 @@ __device__ __forceinline__ uint4 rope_chunk(const uint4 &x, const uint4 &cs, con
 }
 
 // Hides a value's origin from the optimiser (no code is emitted).
-__device__ __forceinline__ void opaque(uint64_t &x) { asm volatile("" : "+l"(x)); }
+__device__ __forceinline__ void opaque(uint32_t &x) { asm volatile("" : "+r"(x)); }
 
 template <uint32_t kRegs>
 __device__ __forceinline__ void reg_inc() {
@@ -849,17 +849,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = desc_kmajor(sbase + kOffQ, 0);
       const uint64_t dk0 = desc_kmajor(sbase + kOffK, 0);
       const uint64_t dv0 = desc_v(sbase + kOffV, 0);
+      // upper descriptor word, the same for Q, K and V (stride and layout)
+      const uint32_t desc_hi = static_cast<uint32_t>(dq0 >> 32);
+      (void)FLUX_DBG(static_cast<uint32_t>(dk0 >> 32) == desc_hi &&
+                         static_cast<uint32_t>(dv0 >> 32) == desc_hi,
+                     kDbgMmaS);
       auto issue_s = [&](int t, int sk) {
         if (!FLUX_DBG(t >= 0 && t < kQTiles && sk >= 0 && sk < kStages, kDbgMmaS)) return;
-        uint64_t da = desc_advance(dq0, t * kTileBytes);
-        uint64_t db = desc_advance(dk0, sk * kTileBytes);
+        uint32_t da = static_cast<uint32_t>(desc_advance(dq0, t * kTileBytes));
+        uint32_t db = static_cast<uint32_t>(desc_advance(dk0, sk * kTileBytes));
         opaque(da);  // per-MMA descriptors are base + constant, computed here,
         opaque(db);  // not hoisted into registers for every (t, stage, kk)
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBlockBytes + (kk & 3) * 32;
-          mma_ss_elect(tmem + t * 128, desc_advance(da, off), desc_advance(db, off), idesc_qk,
-                       kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * kBlockBytes + (kk & 3) * 32) >> 4;
+          mma_ss_elect(tmem + t * 128, da + off, db + off, desc_hi, idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit_elect(bar(kBarSFull + t));
       };
@@ -882,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < n_tiles; ++j) {
           const int g0 = jt + j;  // global tile of this step
           const int sv = g0 % kStages;
-          uint64_t dv = desc_advance(dv0, sv * kTileBytes);
+          uint32_t dv = static_cast<uint32_t>(desc_advance(dv0, sv * kTileBytes));
           opaque(dv);
           const bool more = j + 1 < n_tiles;
           const int sk = (g0 + 1) % kStages;
@@ -904,8 +908,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (FLUX_DBG(t >= 0 && t < kQTiles && sv >= 0 && sv < kStages, kDbgMmaPV)) {
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                             desc_advance(dv, kk * 2048), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                mma_ts_elect(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, dv + ((kk * 2048) >> 4),
+                             desc_hi, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
             }
             mma_commit_elect(bar(kBarODone + t));
             if (t == kQTiles - 1) mma_commit_elect(bar(kBarVEmpty + sv));

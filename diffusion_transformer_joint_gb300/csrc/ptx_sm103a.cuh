@@ -236,25 +236,37 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 // with compute warps busy on the same SM sub-partition, a warp walking the
 // schedule this way issues MMAs several times faster than a single lane
 // branched off on its own.
-__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
+//
+// The shared-memory descriptors are passed as their two 32-bit words: the
+// lower word holds the start address (and the leading byte offset), the upper
+// one the stride and layout fields, which are the same for every descriptor
+// of a kernel. Stepping through a tile then adds to the lower word only (the
+// address field never carries out of it), one instruction instead of a
+// 64-bit add per operand and MMA.
+__device__ __forceinline__ void mma_ss_elect(uint32_t d_tmem, uint32_t adesc_lo, uint32_t bdesc_lo,
+                                             uint32_t desc_hi, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 ad, bd;\n\t"
+      "mov.b64 ad, {%1, %3};\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(adesc_lo), "r"(bdesc_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
-__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
+__device__ __forceinline__ void mma_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint32_t bdesc_lo,
+                                             uint32_t desc_hi, uint32_t idesc,
+                                             uint32_t accumulate) {
   asm volatile(
-      "{\n\t.reg .pred p, e;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
+      "{\n\t.reg .pred p, e;\n\t.reg .b64 bd;\n\t"
+      "mov.b64 bd, {%2, %3};\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
       "elect.sync _|e, 0xffffffff;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(bdesc_lo), "r"(desc_hi), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
