@@ -11,30 +11,34 @@
 // Persistent: one CTA per SM walks work items (batch, head, 256-row block)
 // round robin; for each it owns 256 query rows (two 128-row tiles Q0, Q1)
 // and walks every 128-key tile, starting at a tile that depends on its row
-// block (spread evenly over the head). The K/V rings, the table ring and
-// every barrier phase run on across items, so the next item's Q is loaded
-// and rotated while the current item's last tiles and epilogue finish.
+// block (spread evenly over the head). The K/V rings and every barrier phase
+// run on across items, so the next item's Q is loaded while the current
+// item's last tiles and epilogue finish.
 // 16 warps in four warpgroups:
-//   WG0  warp 0: TMA producer of raw Q (once), K tiles (2-stage ring) and
-//        the packed (cos, sin) table in 64-token halves (2-buffer ring);
+//   WG0  warp 0: TMA producer of Q and of K tiles (2-stage ring);
 //        warp 1: MMA issuer (the whole warp walks the schedule, elect.sync
 //        picks the issuing lane); warp 2: TMEM allocation;
 //        warp 3: TMA producer of V tiles (2-stage ring).
 //   WG1  softmax of Q0: thread = TMEM lane = query row.
 //   WG2  softmax of Q1.
-//   WG3  RoPE: rotates each landed Q / K tile in place in shared memory,
-//        one adjacent channel pair per 32-bit word, with the table half
-//        that landed beside it, then hands the tile to the MMA.
+//   WG3  RoPE, from a work queue the producer fills: prepares the CTA's next
+//        item (its Q rows and first two K tiles rotated global to global
+//        into the exchange buffer) while the current one runs, and rotates
+//        in shared memory any K tile that no CTA has published yet (one
+//        adjacent channel pair per 32-bit word, table rows staged by TMA).
+// The first item is prepared the same way by all 512 threads before the
+// roles start.
 // Rotated K is shared between the CTAs that work on one head: a CTA that
 // rotates a K tile also stores it to an exchange buffer (a bf16 copy of K's
 // layout) and sets one flag per RoPE warp; a CTA whose producer finds all
 // four flags set for this launch loads the rotated tile from there straight
 // into the K stage (no table, no RoPE warps). Staggered start tiles make
 // the CTAs of a head rotate different tiles first. Without the buffer every
-// CTA rotates every K tile it loads; the results are bit-identical.
-// Every global-to-shared copy is a TMA tile copy (128-byte swizzle for Q, K,
-// V; out-of-range tokens read as zeros); nothing on the path waits on a
-// plain global load.
+// CTA rotates every Q and K tile it loads in shared memory; the results are
+// bit-identical.
+// Every copy into shared memory is a TMA tile copy (128-byte swizzle for Q,
+// K, V; out-of-range tokens read as zeros); only the preparation, off the
+// MMA's path, uses plain global loads.
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,384), O1 [384,512); the
 // softmax writes P_t as packed bf16 over the first 64 columns of S_t and the
 // MMA reads it from there (A operand in TMEM).
