@@ -708,12 +708,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int span = (n_tiles - prep_at - 2) / kPrepChunks;
         const int gap = span < 1 ? 1 : (span > kPrepMaxGap ? kPrepMaxGap : span);
         for (int j = 0; ok && j < n_tiles; ++j, ++jt) {
-          while (share && next < n_items && pieces < kPrepChunks &&
-                 (j >= prep_at + gap * pieces || j == n_tiles - 1)) {
-            post(kRqPrep | (static_cast<uint32_t>(pieces) << 4), static_cast<uint32_t>(next));
-            ++pieces;
-          }
-          if (!ok) break;
           const int s = jt % kStages;
           const int tj = tile_at(it, j);
           const int krow = static_cast<int>(tile_row(it, tj));
@@ -787,6 +781,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                      (static_cast<uint32_t>(tj) << 9),
                  static_cast<uint32_t>(item));
           }
+          // after this tile's own copy (and its in-place rotation, if any, is
+          // queued ahead of the preparation piece)
+          while (share && next < n_items && pieces < kPrepChunks &&
+                 (j >= prep_at + gap * pieces || j == n_tiles - 1)) {
+            post(kRqPrep | (static_cast<uint32_t>(pieces) << 4), static_cast<uint32_t>(next));
+            ++pieces;
+          }
+          if (!ok) break;
           // the next item's raw Q into L2 a few tiles before it is loaded (with
           // the exchange buffer the RoPE warps have read it long before)
           if (!share && j == (n_tiles > kQPrefetchTiles ? n_tiles - kQPrefetchTiles : 0) &&
