@@ -329,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
                 "pipelining": PIPELINING},
         "gpu_launches": 2 * K,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle baseline is an N = 1 figure
         gpu_out = sets[0][3].float().cpu().numpy()  # the last output of the first input set
         norm_np = None
         if qk_norm is not None:
@@ -798,7 +798,7 @@ def run_proj(args, rank, world, local_rank):
                 "pipelining": PIPELINING},
         "gpu_launches": K,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and world == 1:  # the oracle baseline is an N = 1 figure
         line["cpu_baseline"] = proj_cpu_baseline(w, target_s=args.cpu_seconds)
     return line
 
